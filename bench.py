@@ -1,0 +1,330 @@
+"""Benchmark: SAR image formation (fused range compression + time-domain
+backprojection) on the spotlight scene sized like the pages' example
+(Na = 4096 pulses, Nr = 4096 samples, x8 range upsampling, 1024 x 1024 image
+at 0.25 m, 64 point targets + clutter).
+
+One step = range-compress every pulse, then backproject every pulse into the
+image, through the C ABI (sar_range_compress + sar_backproject, the two
+halves of sar_form_image), with inputs resident in HBM.  Four input sets
+rotate between steps (536 MB of raw echoes, more than the 129 MB L2).  Prints
+one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the oracle is the reference arm: the pages ship
+no code).  Under torchrun every rank forms its own image (independent
+problems, weak scaling, no collective on the data path).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "backprojection Gpix-pulse/s + range lines/s; % FP32 and % HBM roofline"
+UNIT = "Gpix-pulse/s"
+CONFIG_ID = 3
+FLOPS_PER_PIXEL_PULSE = 30          # range 9, index 4, interpolation 6, phase 3, complex MAC 8
+PAGES_BP_GPIX_PULSE_S = 4096 * 1024 * 1024 / 0.8 / 1e9   # RTX 3080, BP only, same workload (context)
+
+
+def rank_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_traffic(kernel, src_file):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        with open(src_file, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        if rec.get("source_sha256") == digest:
+            return rec.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import domain_backprojection_gb300 as sar
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = synth.CONFIGS[CONFIG_ID]
+    scene = synth.make_scene(CONFIG_ID, device=dev)
+    radar, grid = scene["radar"], scene["grid"]
+    plan = sar.sar_plan_create(radar, grid, local_rank)
+    n_sets = 4
+    raws = [scene["raw"]] + [scene["raw"].clone() for _ in range(n_sets - 1)]
+    poss = [scene["pos"]] + [scene["pos"].clone() for _ in range(n_sets - 1)]
+    rc = torch.empty(cfg.n_pulses, radar.n_range * radar.upsample, dtype=torch.complex64, device=dev)
+    img = torch.empty(grid.ny, grid.nx, dtype=torch.complex64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sar.sar_range_compress(plan, raws[i % n_sets], rc, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        sar.sar_backproject(plan, rc, poss[i % n_sets], 0, cfg.n_pulses, img, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    sar.sar_plan_sync(plan, stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches = 0
+    with ClockSampler(local_rank) as clocks:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+            launches += 1 + sar.sar_plan_last_launches(plan)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+    sar.sar_plan_sync(plan, stream)
+    ms_total = t0.elapsed_time(t1)
+    rc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    pp = cfg.pixel_pulses
+    value = world * pp / (ms_step * 1e-3) / 1e9
+
+    # end to end through the host-buffer entry point: H2D of raw + positions, both kernels, D2H of the image
+    raw_h = scene["raw"].cpu().pin_memory()
+    pos_h = scene["pos"].cpu().pin_memory()
+    img_h = torch.empty(grid.ny, grid.nx, dtype=torch.complex64, pin_memory=True)
+    for _ in range(2):
+        sar.sar_form_image_host(plan, raw_h, pos_h, img_h)
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize(dev)
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        sar.sar_form_image_host(plan, raw_h, pos_h, img_h)
+    e2e_s = (time.perf_counter() - w0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank != 0:
+        return None
+    props = torch.cuda.get_device_properties(dev)
+    peaks, peak_src = measured_peaks()
+    clk = clocks.summary()
+    sm_mhz = clk["sm_mhz"] if clk else float(peaks.get("clocks_under_load", {}).get("sm_mhz_median", 1455.0))
+    fp32_peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12      # TFLOP/s at the sampled clock
+    fp32_peak_max = props.multi_processor_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+    bp_tflops = FLOPS_PER_PIXEL_PULSE * pp / (bp_ms * 1e-3) / 1e12
+    n_range, U = radar.n_range, radar.upsample
+    rc_bytes = cfg.n_pulses * 8 * n_range * (1 + U)
+    rc_gbs = rc_bytes / (rc_ms * 1e-3) / 1e9
+    src = os.path.join(ROOT, "domain_backprojection_gb300", "csrc")
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": round(value / PAGES_BP_GPIX_PULSE_S, 2), "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"spotlight-3deg: Na={cfg.n_pulses} Nr={n_range} U={U} image {grid.nx}x{grid.ny}"
+                               f" @ {grid.dx} m, 64 targets + 16384 clutter scatterers",
+                   "pixel_pulses_per_step": pp, "range_lines_per_step": cfg.n_pulses,
+                   "l2": "4 rotating input sets (536 MB raw) > 129 MB L2; 1.07 GB compressed lines per step",
+                   "step": "sar_range_compress + sar_backproject (= sar_form_image)"},
+        "rc_lines_per_s": round(world * cfg.n_pulses / (rc_ms * 1e-3), 1),
+        "bp_gpix_pulse_per_s": round(world * pp / (bp_ms * 1e-3) / 1e9, 3),
+        "kernel_ms": {"rc_fused_kernel": round(rc_ms, 4), "bp_kernel": round(bp_ms, 4)},
+        "roofline": {"kernel": "bp_kernel", "bound": "alu", "achieved": round(bp_tflops, 3),
+                     "peak": round(fp32_peak, 3), "unit": "TFLOP/s", "frac": round(bp_tflops / fp32_peak, 4),
+                     "traffic": kernel_traffic("bp_kernel", os.path.join(src, "bp_kernel.cu")),
+                     "peak_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz "
+                                   f"(median SM clock sampled during the timed region)",
+                     "frac_of_max_clock_peak": round(bp_tflops / fp32_peak_max, 4),
+                     "flops_per_pixel_pulse": FLOPS_PER_PIXEL_PULSE},
+        "roofline_rc": {"kernel": "rc_fused_kernel", "bound": "hbm", "achieved": round(rc_gbs, 1),
+                        "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
+                        "frac": round(rc_gbs / float(peaks.get("hbm_gbs", 6800.0)), 4),
+                        "traffic": kernel_traffic("rc_fused_kernel", os.path.join(src, "rc_kernel.cu")),
+                        "peak_source": peak_src, "algorithmic_bytes_per_line": 8 * n_range * (1 + U)},
+        "clocks": clk,
+        "e2e": {"value": round(world * pp / e2e_s / 1e9, 3), "unit": UNIT,
+                "h2d_bytes_per_step": raw_h.numel() * 8 + pos_h.numel() * 8,
+                "d2h_bytes_per_step": img_h.numel() * 8, "api": "sar_form_image_host"},
+        "gpu_launches": launches,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(scene, budget_s=args.cpu_seconds)
+    return out
+
+
+def cpu_baseline(scene, budget_s=12.0, threads=None):
+    """The fp64 oracle, as it stands, on the host cores, on a bounded sample of the
+    step: the first 512 pulses (their range compression, and backprojection of a
+    square pixel patch that grows until it takes about half the budget), scaled
+    to all pulses and all pixels."""
+    import numpy as np
+    import oracle
+
+    threads = threads or os.cpu_count()
+    radar, grid = scene["radar"], scene["grid"]
+    na = scene["raw"].shape[0]
+    n_s = min(512, na)
+    raw = scene["raw"][:n_s].cpu().numpy()
+    pos = scene["pos"][:n_s].cpu().numpy()
+    oracle.lib()
+    t = time.perf_counter()
+    rc = oracle.range_compress(radar, raw, threads=threads)
+    rc_s = time.perf_counter() - t
+    cy, cx = grid.ny // 2, grid.nx // 2
+    side = 16
+    while True:
+        pix = np.array([(cy + dy) * grid.nx + cx + dx for dy in range(-side // 2, side // 2)
+                        for dx in range(-side // 2, side // 2)], dtype=np.int64)
+        t = time.perf_counter()
+        oracle.backproject(radar, grid, rc, pos, pulse_begin=0, pulse_count=n_s, pixels=pix, threads=threads)
+        bp_s = time.perf_counter() - t
+        if bp_s > 0.5 * budget_s or side >= min(grid.nx, grid.ny):
+            break
+        side *= 2
+    full_s = (rc_s + bp_s * grid.nx * grid.ny / pix.size) * na / n_s
+    pp = na * grid.nx * grid.ny
+    return {"value": round(pp / full_s / 1e9, 5), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n_s} of {na} pulses: their range compression ({rc_s:.2f} s) and backprojection of a "
+                      f"{side}x{side} pixel patch ({bp_s:.2f} s), scaled to {na} pulses and the "
+                      f"{grid.nx}x{grid.ny} image; fp64, {threads} threads",
+            "est_full_step_s": round(full_s, 2)}
+
+
+def run_reference(args, rank, world, local_rank):
+    import synth
+    import torch
+
+    if rank != 0:
+        return None
+    scene = synth.make_scene(CONFIG_ID, device="cuda" if torch.cuda.is_available() else "cpu")
+    per_step = max(1.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(scene, budget_s=per_step)
+    runs = [cpu_baseline(scene, budget_s=per_step) for _ in range(args.steps)]
+    vals = [r["value"] for r in runs]
+    cb = dict(runs[-1])
+    v = statistics.median(vals)
+    cfg = synth.CONFIGS[CONFIG_ID]
+    ms = cfg.pixel_pulses / (v * 1e9) * 1e3
+    cb["value"] = round(v, 5)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"spotlight-3deg: Na={cfg.n_pulses} Nr={cfg.n_range} U={cfg.upsample} image "
+                                   f"{cfg.nx}x{cfg.ny} @ {cfg.pixel} m (bounded sample per step, scaled)"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local_rank = rank_env()
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = (run_reference if args.impl == "reference" else run_ours)(args, rank, world, local_rank)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,429 @@
+// sar_api.cu -- the C ABI declared in include/sar.h: plan creation (argument
+// validation, matched-filter and transform tables in float64 on the host),
+// range compression, backprojection and image formation entry points.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "sar_internal.cuh"
+
+struct sar_plan_s {
+    int device = 0;
+    sar_radar radar{};
+    sar_grid grid{};
+    bool has_grid = false;
+    bool check_bounds = false;
+    // range compression
+    sar::RcArgs rc{};
+    float2 *d_tables = nullptr;       // H | tw | ptw_hi | ptw_lo in one allocation
+    // backprojection
+    sar::BpArgs bp{};
+    // device error word and its pinned host mirror
+    int *d_err = nullptr;
+    int *h_err = nullptr;
+    // buffers for the host-pointer entry point (allocated on first use)
+    void *d_raw = nullptr, *d_pos = nullptr, *d_rc = nullptr, *d_img = nullptr;
+    int32_t last_launches = 0;
+};
+
+namespace {
+
+using sar::kC0;
+
+struct DeviceGuard {
+    int prev = -1;
+    cudaError_t status = cudaSuccess;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) status = cudaSetDevice(dev);
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool finite_pos(double v) { return std::isfinite(v) && v > 0.0; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool factor_235(int n)
+{
+    for (int p : {2, 3, 5})
+        while (n % p == 0) n /= p;
+    return n == 1;
+}
+
+// Radix sequence for the Stockham passes: 16s first, then 8, 4, 5, 3, 2.
+int plan_radices(int n, int *radix)
+{
+    int np = 0;
+    while (n % 16 == 0 && n > 16) { radix[np++] = 16; n /= 16; }
+    for (int r : {16, 8, 4, 5, 3, 2})
+        while (n % r == 0 && n > 1) { radix[np++] = r; n /= r; }
+    return np;
+}
+
+int chirp_samples(const sar_radar &r)
+{
+    const double x = r.pulse_width * r.fs;
+    const double k = std::nearbyint(x);
+    return (int)(std::fabs(x - k) < 1e-6 ? k : std::floor(x));
+}
+
+sar_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return SAR_OK;
+    if (e == cudaErrorMemoryAllocation) return SAR_ERR_NO_MEMORY;
+    return SAR_ERR_CUDA;
+}
+
+// The matched-filter spectrum conj(DFT_N(h)), h the centred up-chirp on the
+// integer samples s with -nc/2 <= s < nc/2, stored circularly; the DFT is a
+// direct sum over the nc nonzero samples, in float64.
+void build_matched_filter(const sar_radar &r, int n, std::vector<float2> &H)
+{
+    const int nc = chirp_samples(r);
+    const double K = r.bandwidth / r.pulse_width;
+    std::vector<double> hre, him;
+    std::vector<int> hs;
+    for (int s = -nc; s <= nc; s++) {
+        if (2 * s < -nc || 2 * s >= nc) continue;
+        const double tau = s / r.fs;
+        const double ph = M_PI * K * tau * tau;
+        hs.push_back(((s % n) + n) % n);
+        hre.push_back(std::cos(ph));
+        him.push_back(std::sin(ph));
+    }
+    H.resize(n);
+    for (int k = 0; k < n; k++) {
+        double re = 0.0, im = 0.0;
+        for (size_t j = 0; j < hs.size(); j++) {
+            const long long t = ((long long)hs[j] * k) % n;
+            const double a = -2.0 * M_PI * (double)t / n;
+            const double c = std::cos(a), s = std::sin(a);
+            re += hre[j] * c - him[j] * s;
+            im += hre[j] * s + him[j] * c;
+        }
+        H[k] = make_float2((float)re, (float)-im);     // conjugate
+    }
+}
+
+sar_status validate_radar(const sar_radar *r)
+{
+    if (!r) return SAR_ERR_INVALID_ARG;
+    if (!finite_pos(r->fc) || !finite_pos(r->bandwidth) || !finite_pos(r->pulse_width) || !finite_pos(r->fs) ||
+        !std::isfinite(r->range_start))
+        return SAR_ERR_INVALID_ARG;
+    if (r->n_pulses < 1 || r->n_range < 1 || r->upsample < 1) return SAR_ERR_INVALID_ARG;
+    if (r->n_range < 16 || r->n_range > 8192 || (r->n_range & 1) || !factor_235(r->n_range)) return SAR_ERR_UNSUPPORTED;
+    if (r->upsample != 1 && r->upsample != 2 && r->upsample != 4 && r->upsample != 8) return SAR_ERR_UNSUPPORTED;
+    const int nc = chirp_samples(*r);
+    if (nc < 1 || nc > r->n_range) return SAR_ERR_UNSUPPORTED;
+    return SAR_OK;
+}
+
+sar_status validate_grid(const sar_grid *g)
+{
+    if (!std::isfinite(g->x0) || !std::isfinite(g->y0) || !std::isfinite(g->z0)) return SAR_ERR_INVALID_ARG;
+    if (!finite_pos(g->dx) || !finite_pos(g->dy) || g->nx < 1 || g->ny < 1) return SAR_ERR_INVALID_ARG;
+    return SAR_OK;
+}
+
+sar_status setup_rc(sar_plan p)
+{
+    const sar_radar &r = p->radar;
+    const int n = r.n_range, U = r.upsample, un = n * U;
+    sar::RcArgs &a = p->rc;
+    a.n = n;
+    a.u = U;
+    a.n_passes = plan_radices(n, a.radix);
+    a.inv_n = (float)(1.0 / n);
+    int bits = 0;
+    while ((1 << (2 * bits)) < un) bits++;                      // lo table ~ sqrt(U N) entries
+    a.ptw_lo_bits = bits;
+    const int n_lo = 1 << bits, n_hi = (un + n_lo - 1) / n_lo;
+
+    std::vector<float2> host;
+    build_matched_filter(r, n, host);                           // [0, n)
+    for (int t = 0; t < n; t++) {                               // [n, 2n)
+        const double ang = -2.0 * M_PI * t / n;
+        host.push_back(make_float2((float)std::cos(ang), (float)std::sin(ang)));
+    }
+    for (int t = 0; t < n_hi; t++) {                            // [2n, 2n + n_hi)
+        const double ang = -2.0 * M_PI * ((double)t * n_lo) / un;
+        host.push_back(make_float2((float)std::cos(ang), (float)std::sin(ang)));
+    }
+    for (int t = 0; t < n_lo; t++) {                            // then n_lo
+        const double ang = -2.0 * M_PI * (double)t / un;
+        host.push_back(make_float2((float)std::cos(ang), (float)std::sin(ang)));
+    }
+    cudaError_t e = cudaMalloc(&p->d_tables, host.size() * sizeof(float2));
+    if (e != cudaSuccess) return cuda_status(e);
+    e = cudaMemcpy(p->d_tables, host.data(), host.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_status(e);
+    a.h = p->d_tables;
+    a.tw = p->d_tables + n;
+    a.ptw_hi = p->d_tables + 2 * n;
+    a.ptw_lo = p->d_tables + 2 * n + n_hi;
+    return cuda_status(sar::rc_configure(n));
+}
+
+sar_status setup_bp(sar_plan p)
+{
+    const sar_radar &r = p->radar;
+    const sar_grid &g = p->grid;
+    sar::BpArgs &a = p->bp;
+    a.x0 = g.x0;
+    a.y0 = g.y0;
+    a.z0 = g.z0;
+    a.dx = (float)g.dx;
+    a.dy = (float)g.dy;
+    a.nx = g.nx;
+    a.ny = g.ny;
+    a.tiles_x = (g.nx + sar::kBpTileX - 1) / sar::kBpTileX;
+    a.tiles_y = (g.ny + sar::kBpTileY - 1) / sar::kBpTileY;
+    if (a.tiles_y > 65535) return SAR_ERR_UNSUPPORTED;
+    const double dr = kC0 / (2.0 * r.fs * r.upsample);
+    a.range_start = r.range_start;
+    a.inv_dr = 1.0 / dr;
+    a.dr = (float)dr;
+    a.n_samples = r.n_range * r.upsample;
+    const double lambda = kC0 / r.fc;
+    const double ph = 2.0 * r.range_start / lambda;
+    a.phase0_turns = ph - std::floor(ph);
+    a.kappa = 2.0 * dr / lambda;
+    a.two_pi_kappa = (float)(2.0 * M_PI * a.kappa);
+    // window: every pixel of a tile lies within the half-diagonal r_t of its centre, so its range lies
+    // within r_t of the centre's range; wh bins on each side plus margin for the float32 offsets
+    const double ex = (sar::kBpTileX - 1) * g.dx, ey = (sar::kBpTileY - 1) * g.dy;
+    const double rt = 0.5 * std::sqrt(ex * ex + ey * ey);
+    a.wh = (int)std::ceil(rt / dr) + 3;
+    a.w = 2 * a.wh + 1;
+    a.min_range_tiles = (float)(100.0 * rt);
+    // pulses per batch: as many as fit 64 KB of staging (three CTAs per SM), between 4 and 32
+    int pb = (int)((64 * 1024) / ((size_t)a.w * sizeof(float4) + 36));
+    if (pb > 32) pb = 32;
+    if (pb < 4) {
+        pb = 4;
+        if (sar::bp_smem_bytes(a.w, pb) > 96 * 1024) return SAR_ERR_UNSUPPORTED;   // pixels too coarse for a tile
+    }
+    a.pulses_per_batch = pb;
+    a.err = p->d_err;
+    return cuda_status(sar::bp_configure());
+}
+
+void free_plan(sar_plan p)
+{
+    if (!p) return;
+    cudaFree(p->d_tables);
+    cudaFree(p->d_err);
+    if (p->h_err) cudaFreeHost(p->h_err);
+    cudaFree(p->d_raw);
+    cudaFree(p->d_pos);
+    cudaFree(p->d_rc);
+    cudaFree(p->d_img);
+    delete p;
+}
+
+sar_status do_backproject(sar_plan plan, const void *rc, const double *pos, int32_t pulse_begin,
+                          int32_t pulse_count, void *image, int accumulate, cudaStream_t s)
+{
+    const size_t img_bytes = (size_t)plan->grid.nx * plan->grid.ny * sizeof(float2);
+    if (pulse_count == 0) {
+        if (!accumulate) return cuda_status(cudaMemsetAsync(image, 0, img_bytes, s));
+        return SAR_OK;
+    }
+    sar::BpArgs a = plan->bp;
+    a.rc = static_cast<const float2 *>(rc);
+    a.pos = pos;
+    a.image = static_cast<float2 *>(image);
+    a.pulse_begin = pulse_begin;
+    a.pulse_end = pulse_begin + pulse_count;
+    a.accumulate = accumulate ? 1 : 0;
+    plan->last_launches += 1;
+    return cuda_status(sar::launch_bp(a, plan->check_bounds, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sar_status_string(sar_status s)
+{
+    switch (s) {
+    case SAR_OK: return "success";
+    case SAR_ERR_INVALID_ARG: return "invalid argument";
+    case SAR_ERR_UNSUPPORTED: return "unsupported parameters";
+    case SAR_ERR_NO_MEMORY: return "out of memory";
+    case SAR_ERR_CUDA: return "CUDA error";
+    case SAR_ERR_TIMEOUT: return "device-side wait timed out";
+    case SAR_ERR_INTERNAL: return "internal error (device bounds check)";
+    }
+    return "unknown status";
+}
+
+sar_status sar_plan_create(const sar_radar *radar, const sar_grid *grid, int device, sar_plan *out)
+{
+    if (!out) return SAR_ERR_INVALID_ARG;
+    *out = nullptr;
+    sar_status st = validate_radar(radar);
+    if (st != SAR_OK) return st;
+    if (grid && (st = validate_grid(grid)) != SAR_OK) return st;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) return SAR_ERR_CUDA;
+    if (device < 0 || device >= ndev) return SAR_ERR_INVALID_ARG;
+    DeviceGuard guard(device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+
+    sar_plan p = new (std::nothrow) sar_plan_s;
+    if (!p) return SAR_ERR_NO_MEMORY;
+    p->device = device;
+    p->radar = *radar;
+    if (grid) {
+        p->grid = *grid;
+        p->has_grid = true;
+    }
+    const char *cb = std::getenv("SAR_CHECK_BOUNDS");
+    p->check_bounds = cb && cb[0] == '1';
+    cudaError_t e = cudaMalloc(&p->d_err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMallocHost(&p->h_err, sizeof(int));
+    if (e != cudaSuccess) {
+        free_plan(p);
+        return cuda_status(e);
+    }
+    st = setup_rc(p);
+    if (st == SAR_OK && p->has_grid) st = setup_bp(p);
+    if (st != SAR_OK) {
+        free_plan(p);
+        return st;
+    }
+    *out = p;
+    return SAR_OK;
+}
+
+sar_status sar_plan_destroy(sar_plan plan)
+{
+    if (!plan) return SAR_OK;
+    DeviceGuard guard(plan->device);
+    cudaDeviceSynchronize();
+    free_plan(plan);
+    return SAR_OK;
+}
+
+sar_status sar_workspace_size(sar_plan plan, size_t *bytes)
+{
+    if (!plan || !bytes) return SAR_ERR_INVALID_ARG;
+    const size_t raw = (size_t)plan->radar.n_pulses * plan->radar.n_range * plan->radar.upsample * sizeof(float2);
+    *bytes = (raw + 255) & ~(size_t)255;
+    return SAR_OK;
+}
+
+sar_status sar_range_compress(sar_plan plan, const void *raw, void *rc, int64_t n_lines, void *stream)
+{
+    if (!plan || !raw || !rc || n_lines < 1) return SAR_ERR_INVALID_ARG;
+    if (!aligned16(raw) || !aligned16(rc)) return SAR_ERR_INVALID_ARG;
+    const int64_t in_bytes = n_lines * plan->radar.n_range * (int64_t)sizeof(float2);
+    const int64_t out_bytes = in_bytes * plan->radar.upsample;
+    const char *r0 = static_cast<const char *>(raw), *c0 = static_cast<const char *>(rc);
+    if (r0 < c0 + out_bytes && c0 < r0 + in_bytes) return SAR_ERR_INVALID_ARG;     // overlap
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    plan->last_launches = 1;
+    return cuda_status(sar::launch_rc(plan->rc, static_cast<const float2 *>(raw), static_cast<float2 *>(rc), n_lines,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+sar_status sar_backproject(sar_plan plan, const void *rc, const double *pos, int32_t pulse_begin,
+                           int32_t pulse_count, void *image, int accumulate, void *stream)
+{
+    if (!plan || !rc || !pos || !image) return SAR_ERR_INVALID_ARG;
+    if (!plan->has_grid) return SAR_ERR_UNSUPPORTED;
+    if (pulse_begin < 0 || pulse_count < 0 || (int64_t)pulse_begin + pulse_count > plan->radar.n_pulses)
+        return SAR_ERR_INVALID_ARG;
+    if (!aligned16(rc) || !aligned16(image) || (reinterpret_cast<uintptr_t>(pos) & 7u)) return SAR_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    plan->last_launches = 0;
+    return do_backproject(plan, rc, pos, pulse_begin, pulse_count, image, accumulate,
+                          static_cast<cudaStream_t>(stream));
+}
+
+sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, void *image, void *workspace,
+                          size_t workspace_bytes, void *stream)
+{
+    if (!plan || !raw || !pos || !image || !workspace) return SAR_ERR_INVALID_ARG;
+    if (!plan->has_grid) return SAR_ERR_UNSUPPORTED;
+    size_t need = 0;
+    sar_workspace_size(plan, &need);
+    if (workspace_bytes < need) return SAR_ERR_INVALID_ARG;
+    if (!aligned16(raw) || !aligned16(workspace) || !aligned16(image) || (reinterpret_cast<uintptr_t>(pos) & 7u))
+        return SAR_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    plan->last_launches = 1;
+    sar_status st = cuda_status(sar::launch_rc(plan->rc, static_cast<const float2 *>(raw),
+                                               static_cast<float2 *>(workspace), plan->radar.n_pulses, s));
+    if (st != SAR_OK) return st;
+    return do_backproject(plan, workspace, pos, 0, plan->radar.n_pulses, image, 0, s);
+}
+
+sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double *pos_host, void *image_host,
+                               void *stream)
+{
+    if (!plan || !raw_host || !pos_host || !image_host) return SAR_ERR_INVALID_ARG;
+    if (!plan->has_grid) return SAR_ERR_UNSUPPORTED;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    const sar_radar &r = plan->radar;
+    const size_t raw_bytes = (size_t)r.n_pulses * r.n_range * sizeof(float2);
+    const size_t pos_bytes = (size_t)r.n_pulses * 3 * sizeof(double);
+    const size_t img_bytes = (size_t)plan->grid.nx * plan->grid.ny * sizeof(float2);
+    size_t ws = 0;
+    sar_workspace_size(plan, &ws);
+    cudaError_t e = cudaSuccess;
+    if (!plan->d_raw && e == cudaSuccess) e = cudaMalloc(&plan->d_raw, raw_bytes);
+    if (!plan->d_pos && e == cudaSuccess) e = cudaMalloc(&plan->d_pos, pos_bytes);
+    if (!plan->d_rc && e == cudaSuccess) e = cudaMalloc(&plan->d_rc, ws);
+    if (!plan->d_img && e == cudaSuccess) e = cudaMalloc(&plan->d_img, img_bytes);
+    if (e != cudaSuccess) return cuda_status(e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = cudaMemcpyAsync(plan->d_raw, raw_host, raw_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(plan->d_pos, pos_host, pos_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    sar_status st = sar_form_image(plan, plan->d_raw, static_cast<const double *>(plan->d_pos), plan->d_img,
+                                   plan->d_rc, ws, stream);
+    if (st != SAR_OK) return st;
+    e = cudaMemcpyAsync(image_host, plan->d_img, img_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_status(e);
+}
+
+sar_status sar_plan_sync(sar_plan plan, void *stream)
+{
+    if (!plan) return SAR_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return SAR_ERR_CUDA;
+    e = cudaMemcpy(plan->h_err, plan->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return SAR_ERR_CUDA;
+    const int flags = *plan->h_err;
+    if (flags) {
+        e = cudaMemset(plan->d_err, 0, sizeof(int));
+        if (e != cudaSuccess) return SAR_ERR_CUDA;
+    }
+    if (flags & sar::kDevErrBounds) return SAR_ERR_INTERNAL;
+    if (flags & sar::kDevErrGeometry) return SAR_ERR_UNSUPPORTED;
+    return SAR_OK;
+}
+
+int32_t sar_plan_last_launches(sar_plan plan) { return plan ? plan->last_launches : 0; }
+
+}  // extern "C"

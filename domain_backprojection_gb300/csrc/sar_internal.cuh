@@ -1,0 +1,77 @@
+// sar_internal.cuh -- declarations shared by the library's translation units
+// (plan / ABI code, the range-compression kernel and the backprojection kernel).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sar.h"
+
+namespace sar {
+
+constexpr double kC0 = 299792458.0;
+constexpr int kMaxPasses = 16;
+
+// Device-side error flags (bit mask in the plan's error word).
+enum : int {
+    kDevErrBounds = 1,       // a staged-window index fell outside the window (bounds-checked build)
+    kDevErrGeometry = 2,     // a tile came too close to the antenna for the range expansion
+};
+
+// ----------------------------------------------------------- range compression
+struct RcArgs {
+    int n;                   // samples per line, Nr
+    int u;                   // upsampling factor U
+    int n_passes;            // Stockham passes of the Nr-point transform
+    int radix[kMaxPasses];   // radix of each pass (product = Nr)
+    int ptw_lo_bits;         // polyphase twiddle t = hi * 2^bits + lo
+    float inv_n;             // 1 / Nr (IDFT scaling: U * 1/(U Nr))
+    const float2 *h;         // matched filter spectrum H[k] = conj(DFT_N chirp)[k], natural order
+    const float2 *tw;        // w_N^t = exp(-2 pi i t / Nr), t in [0, Nr)
+    const float2 *ptw_hi;    // exp(-2 pi i (hi << bits) / (U Nr))
+    const float2 *ptw_lo;    // exp(-2 pi i lo / (U Nr)), lo < 2^bits
+};
+
+int rc_block_threads(int n);
+size_t rc_smem_bytes(int n);
+cudaError_t rc_configure(int n);
+cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s);
+
+// ----------------------------------------------------------- backprojection
+constexpr int kBpTileX = 32;     // pixels per tile along x (one warp lane each)
+constexpr int kBpTileY = 32;     // pixels per tile along y
+constexpr int kBpRowsPerThread = 4;
+constexpr int kBpThreads = kBpTileX * kBpTileY / kBpRowsPerThread;   // 256
+
+struct BpArgs {
+    // grid
+    double x0, y0, z0;
+    float dx, dy;
+    int nx, ny, tiles_x, tiles_y;
+    // range axis
+    double range_start;      // m
+    double inv_dr;           // 1 / dr_U (bins per metre)
+    float dr;                // dr_U, m
+    int n_samples;           // U * Nr
+    // phase: exp(+j 2 pi [ (2/lambda) R_start + kappa Q ]) for a fractional global bin Q
+    double phase0_turns;     // frac((2 / lambda) * range_start)
+    double kappa;            // 2 dr_U / lambda, turns per bin
+    float two_pi_kappa;      // 2 pi kappa (rad per bin)
+    // staged window: entries e in [0, w) hold local bins i = e - wh
+    int wh, w;
+    int pulses_per_batch;
+    float min_range_tiles;   // geometry validity: range >= this (m) per tile
+    // data
+    const float2 *rc;        // [Na][U Nr]
+    const double *pos;       // [Na][3]
+    float2 *image;           // [ny][nx]
+    int pulse_begin, pulse_end;
+    int accumulate;
+    int *err;                // device error word
+};
+
+size_t bp_smem_bytes(int w, int pulses_per_batch);
+cudaError_t bp_configure();
+cudaError_t launch_bp(const BpArgs &a, bool check_bounds, cudaStream_t s);
+
+}  // namespace sar

@@ -1,0 +1,147 @@
+/*
+ * sar.h -- C ABI of the GB300 (sm_103a) SAR image-formation library: fused
+ * range compression and time-domain backprojection.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Complex samples are complex64: interleaved (re, im) float32 pairs.
+ *  - Device buffers are CUDA device pointers on the plan's device, 16-byte
+ *    aligned, dense (no row padding).  The caller owns them; the library never
+ *    frees or retains them past the call.
+ *  - Every call that launches work enqueues it on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and returns without synchronising,
+ *    except where stated.  Argument errors are detected before anything is
+ *    launched.  Device-side error flags (bounds checks, geometry validity)
+ *    are reported by sar_plan_sync.
+ *  - Errors are return codes only; nothing aborts, traps or throws.
+ *  - A plan may be used from one host thread at a time.  Calls on different
+ *    streams that share one plan are serialised by the caller.
+ *
+ * Geometry: x along-track, y ground range, z up (metres).  Pixel (ix, iy) sits
+ * at (x0 + ix dx, y0 + iy dy, z0); images are [ny][nx], x fastest.  Antenna
+ * positions are one (x, y, z) float64 triple per pulse (stop-and-go).
+ */
+#ifndef SAR_H
+#define SAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct sar_plan_s *sar_plan;
+
+typedef enum {
+    SAR_OK = 0,
+    SAR_ERR_INVALID_ARG = 1,   /* NULL, non-positive or non-finite values, misaligned pointers, bad ranges */
+    SAR_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle (see each entry) */
+    SAR_ERR_NO_MEMORY = 3,     /* a device or host allocation failed */
+    SAR_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    SAR_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
+    SAR_ERR_INTERNAL = 6       /* a device-side bounds check fired (bug) */
+} sar_status;
+
+/* Radar and sampling parameters.
+ * The transmitted pulse is a baseband linear-FM up-chirp exp(j pi K t^2),
+ * K = bandwidth / pulse_width, on -pulse_width/2 <= t < pulse_width/2; echoes are
+ * sampled at fs starting at two-way time 2 range_start / c0.  Range compression
+ * ("GPU-accelerated backprojection SAR imaging", section 3.1; "Fused FFT ->
+ * filter -> IFFT for SAR on Apple Silicon", section 3.1) produces upsample x
+ * oversampled compressed lines. */
+typedef struct {
+    double fc;            /* carrier frequency, Hz (> 0) */
+    double bandwidth;     /* chirp bandwidth B, Hz (> 0) */
+    double pulse_width;   /* chirp duration Tp, s (> 0); Tp * fs must not exceed n_range */
+    double fs;            /* complex sampling rate, Hz (> 0) */
+    double range_start;   /* slant range of sample 0, m */
+    int32_t n_pulses;     /* pulses Na (>= 1) */
+    int32_t n_range;      /* samples per pulse Nr: even, of the form 2^a 3^b 5^c, 16 <= Nr <= 8192 */
+    int32_t upsample;     /* range upsampling U in {1, 2, 4, 8} */
+} sar_radar;
+
+/* The image grid of pixel centres ("GPU-accelerated backprojection SAR imaging",
+ * section 3.3: pixels on a plane z = z0, mapped from thread indices). */
+typedef struct {
+    double x0, y0, z0;    /* position of pixel (0, 0), m */
+    double dx, dy;        /* pixel spacing, m (> 0) */
+    int32_t nx, ny;       /* pixels per row and rows (>= 1) */
+} sar_grid;
+
+/* Create a plan on CUDA device `device`: validates the parameters, builds the
+ * matched-filter spectrum conj(DFT_Nr(chirp)) and the transform tables in
+ * float64 on the host, uploads them, and allocates the plan's small device
+ * state.  `grid` may be NULL for a range-compression-only plan.
+ * Returns SAR_ERR_INVALID_ARG / SAR_ERR_UNSUPPORTED for bad parameters,
+ * SAR_ERR_NO_MEMORY or SAR_ERR_CUDA on allocation / runtime failure.  On
+ * success *out owns everything the plan allocated. */
+sar_status sar_plan_create(const sar_radar *radar, const sar_grid *grid, int device, sar_plan *out);
+
+/* Free everything the plan owns (synchronises the plan's device first).
+ * NULL is accepted and ignored. */
+sar_status sar_plan_destroy(sar_plan plan);
+
+/* Bytes of caller-provided workspace sar_form_image needs: the compressed
+ * lines, Na * U * Nr complex64, rounded up to 256 bytes. */
+sar_status sar_workspace_size(sar_plan plan, size_t *bytes);
+
+/* Range compression of n_lines pulses, each fused into one kernel pass
+ * ("Fused FFT -> filter -> IFFT for SAR on Apple Silicon", sections 3.1-3.2;
+ * "GPU-accelerated backprojection SAR imaging", section 3.1):
+ *   X = DFT_Nr(raw_n); Y = X * conj(DFT_Nr(chirp)); Y zero-padded to U Nr
+ *   points (bins k with 2k >= Nr at the negative-frequency end);
+ *   rc_n = U * IDFT_{U Nr}(Y')   (so rc_n[U m] is the plain compressed sample m).
+ * raw: device [n_lines][Nr] complex64.  rc: device [n_lines][U Nr] complex64.
+ * 1 <= n_lines; raw and rc must not overlap. */
+sar_status sar_range_compress(sar_plan plan, const void *raw, void *rc, int64_t n_lines, void *stream);
+
+/* Time-domain backprojection of pulses [pulse_begin, pulse_begin + pulse_count)
+ * ("GPU-accelerated backprojection SAR imaging", sections 1.1, 2.2, 3.3): for
+ * every pixel p,
+ *   I(p) = sum_n L_n((|p - a_n| - range_start) / dr_U) * exp(+j 4 pi fc |p - a_n| / c0)
+ * with dr_U = c0 / (2 fs U), L_n the linear interpolation of compressed line n,
+ * and samples outside [0, U Nr) taken as zero.  accumulate != 0 adds into image
+ * instead of overwriting it.  The sum over pulses runs in float32.
+ * rc: device [Na][U Nr] complex64 (full plan-sized array; lines outside the
+ * pulse range are not read).  pos: device [Na][3] float64.  image: device
+ * [ny][nx] complex64.  Needs a plan created with a grid; SAR_ERR_UNSUPPORTED
+ * otherwise.  The kernel computes each pixel's range as a float32 offset
+ * from a float64 range to the centre of its pixel tile; sar_plan_sync reports
+ * SAR_ERR_UNSUPPORTED if a tile came closer to the antenna than the
+ * expansion allows (range below 100 tile half-diagonals). */
+sar_status sar_backproject(sar_plan plan, const void *rc, const double *pos, int32_t pulse_begin,
+                           int32_t pulse_count, void *image, int accumulate, void *stream);
+
+/* Range compression of all Na pulses into `workspace`, then backprojection of
+ * all pulses into `image` (overwritten).  workspace: device, at least
+ * sar_workspace_size bytes.  raw: device [Na][Nr] complex64; pos: device
+ * [Na][3] float64; image: device [ny][nx] complex64. */
+sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, void *image,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* The same image formation from HOST buffers: copies raw and pos to device
+ * buffers the plan owns (allocated on the first call), forms the image and
+ * copies it back to image_host, then synchronises `stream`.  Host buffers
+ * should be pinned for full copy bandwidth.  raw_host: [Na][Nr] complex64;
+ * pos_host: [Na][3] float64; image_host: [ny][nx] complex64. */
+sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double *pos_host, void *image_host,
+                               void *stream);
+
+/* Synchronise `stream`, then read and clear the plan's device error flags:
+ * SAR_ERR_INTERNAL if a bounds check fired, SAR_ERR_UNSUPPORTED if a geometry
+ * validity check failed, SAR_ERR_CUDA on an asynchronous CUDA error. */
+sar_status sar_plan_sync(sar_plan plan, void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *sar_status_string(sar_status status);
+
+/* Number of kernel launches the last call on this plan enqueued (for
+ * accounting in benchmarks); 0 for a NULL plan. */
+int32_t sar_plan_last_launches(sar_plan plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAR_H */

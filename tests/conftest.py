@@ -21,3 +21,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+_SCENES = {}
+
+
+@pytest.fixture(scope="session")
+def scene_cache():
+    """get(cfg) -> a benchmark scene generated on the GPU, keeping only the latest one alive."""
+    import synth
+
+    def get(cfg):
+        if cfg not in _SCENES:
+            _SCENES.clear()
+            _SCENES[cfg] = synth.make_scene(cfg, device="cuda")
+        return _SCENES[cfg]
+    return get

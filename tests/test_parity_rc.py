@@ -1,0 +1,100 @@
+"""GPU range compression (sar_range_compress through the C ABI) against the
+fp64 oracle, element by element, within relative L2 2e-4."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import domain_backprojection_gb300 as sar
+import oracle
+import synth
+from helpers import ORACLE_THREADS, RC_TOL, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _short_pulse_radar(n, U, n_lines):
+    # a 12-sample pulse so that short lines still hold it
+    return synth.Radar(bandwidth=150e6, pulse_width=12 / 180e6, fs=180e6, range_start=5000.0, n_pulses=n_lines,
+                       n_range=n, upsample=U)
+
+
+def _noise(lines, n, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.complex(torch.randn(lines, n, generator=g), torch.randn(lines, n, generator=g))
+
+
+def _run(radar, raw_cpu):
+    plan = sar.sar_plan_create(radar, None, 0)
+    raw = raw_cpu.cuda()
+    rc = sar.sar_range_compress(plan, raw)
+    sar.sar_plan_sync(plan)
+    assert sar.sar_plan_last_launches(plan) == 1
+    return rc.cpu().numpy()
+
+
+@pytest.mark.parametrize("n,U,lines", [
+    (16, 1, 3), (16, 8, 2), (30, 2, 5), (240, 4, 7), (1000, 1, 9), (1000, 8, 3), (1536, 2, 4),
+    (1024, 1, 1), (1024, 8, 37), (2048, 8, 64), (4096, 1, 100), (4096, 8, 16), (6000, 1, 50), (6000, 8, 5),
+    (8192, 1, 33), (8192, 8, 9), (8192, 4, 3), (4050, 2, 3),
+])
+def test_rc_random_lines(n, U, lines):
+    radar = _short_pulse_radar(n, U, lines) if n < 400 else synth.Radar(range_start=5000.0, n_pulses=lines,
+                                                                       n_range=n, upsample=U)
+    raw = _noise(lines, n, n * 10 + U)
+    got = _run(radar, raw)
+    ref = oracle.range_compress(radar, raw.numpy(), threads=ORACLE_THREADS)
+    assert got.shape == ref.shape
+    for i in range(lines):
+        assert rel_l2(got[i], ref[i]) <= RC_TOL, f"line {i}"
+
+
+@pytest.mark.parametrize("nr", synth.RC_SWEEP_NR)
+def test_rc_sweep_full_size(nr):
+    # the range-compression-only workload at its full size (4096 lines), sampled lines checked
+    scene = synth.make_rc_sweep(nr, n_lines=4096, device="cuda")
+    radar = scene["radar"]
+    plan = sar.sar_plan_create(radar, None, 0)
+    rc = sar.sar_range_compress(plan, scene["raw"])
+    sar.sar_plan_sync(plan)
+    sample = np.arange(0, 4096, 61)
+    raw = scene["raw"][sample].cpu().numpy()
+    ref = oracle.range_compress(radar, raw, threads=ORACLE_THREADS)
+    got = rc[sample].cpu().numpy()
+    assert rel_l2(got, ref) <= RC_TOL
+    # each line's compressed chirp peaks at its delay with the line's phase
+    kt = scene["delay_samples"][sample].numpy()
+    pk = np.abs(got).argmax(axis=1)
+    assert np.all(np.abs(pk - kt) <= 0.5 + 1e-9)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_rc_scene_configs_sampled(scene_cache, cfg):
+    c = synth.CONFIGS[cfg]
+    scene = scene_cache(cfg)
+    plan = sar.sar_plan_create(scene["radar"], None, 0)
+    rc = sar.sar_range_compress(plan, scene["raw"])
+    sar.sar_plan_sync(plan)
+    sample = np.linspace(0, c.n_pulses - 1, 12).astype(int)
+    ref = oracle.range_compress(scene["radar"], scene["raw"][sample].cpu().numpy(), threads=ORACLE_THREADS)
+    assert rel_l2(rc[sample].cpu().numpy(), ref) <= RC_TOL
+
+
+def test_rc_subset_of_lines_and_bad_arguments():
+    radar = synth.Radar(range_start=5000.0, n_pulses=64, n_range=2048, upsample=8)
+    plan = sar.sar_plan_create(radar, None, 0)
+    raw = _noise(64, 2048, 3).cuda()
+    full = sar.sar_range_compress(plan, raw)
+    part = sar.sar_range_compress(plan, raw[10:17].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(full[10:17], part)
+    L = sar.lib()
+    import ctypes
+    # n_lines < 1, misaligned, overlapping input/output
+    assert L.sar_range_compress(plan.handle, ctypes.c_void_p(raw.data_ptr()), ctypes.c_void_p(full.data_ptr()), 0,
+                                None) == 1
+    assert L.sar_range_compress(plan.handle, ctypes.c_void_p(raw.data_ptr() + 8), ctypes.c_void_p(full.data_ptr()),
+                                1, None) == 1
+    assert L.sar_range_compress(plan.handle, ctypes.c_void_p(full.data_ptr()), ctypes.c_void_p(full.data_ptr()), 1,
+                                None) == 1
