@@ -6,8 +6,8 @@ from ._binding import (SAR_OK, Plan, SarError, declared_symbols, lib, library_pa
                        sar_form_image, sar_form_image_host, sar_plan_create, sar_plan_destroy,
                        sar_plan_last_launches, sar_plan_sync, sar_range_compress, sar_status_string,
                        sar_workspace_size)
-from .build import build
+from .build import build as build_library
 
-__all__ = ["SAR_OK", "Plan", "SarError", "build", "declared_symbols", "lib", "library_path", "sar_backproject",
+__all__ = ["SAR_OK", "Plan", "SarError", "build_library", "declared_symbols", "lib", "library_path", "sar_backproject",
            "sar_form_image", "sar_form_image_host", "sar_plan_create", "sar_plan_destroy", "sar_plan_last_launches",
            "sar_plan_sync", "sar_range_compress", "sar_status_string", "sar_workspace_size"]

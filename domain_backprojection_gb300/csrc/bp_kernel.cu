@@ -67,12 +67,12 @@ __global__ void __launch_bounds__(kBpThreads, 3) bp_kernel(BpArgs args)
     // tile centre (float64) and this thread's pixel offsets from it (float32)
     const double cx = args.x0 + ((double)tile_x * kBpTileX + 0.5 * (kBpTileX - 1)) * args.dx;
     const double cy = args.y0 + ((double)tile_y * kBpTileY + 0.5 * (kBpTileY - 1)) * args.dy;
-    const float ox = ((float)lane - 0.5f * (kBpTileX - 1)) * args.dx;
+    const float ox = ((float)lane - 0.5f * (kBpTileX - 1)) * args.dxf;
     float oy[kBpRowsPerThread], od2[kBpRowsPerThread];
 #pragma unroll
     for (int k = 0; k < kBpRowsPerThread; k++) {
         const int ly = warp * kBpRowsPerThread + k;
-        oy[k] = ((float)ly - 0.5f * (kBpTileY - 1)) * args.dy;
+        oy[k] = ((float)ly - 0.5f * (kBpTileY - 1)) * args.dyf;
         od2[k] = fmaf(ox, ox, oy[k] * oy[k]);
     }
     float acc_re[kBpRowsPerThread], acc_im[kBpRowsPerThread];
@@ -101,13 +101,16 @@ __global__ void __launch_bounds__(kBpThreads, 3) bp_kernel(BpArgs args)
             // and zero this pulse's parameters: every pixel then reads entry wh, inside the window.
             const bool ok = (r0 >= (double)args.min_range_tiles) && (fabs(qg) < 1.0e9);
             const double o = ok ? floor(qg) : 0.0;
-            const float inv_r0 = 1.0f / (float)r0;
-            const float inv_dr = (float)args.inv_dr;
+            // 1 / (r0 dr) to float64 accuracy: float reciprocal refined by one Newton step
+            const float inv_f = 1.0f / (float)r0;
+            const double inv_r0d = (double)inv_f * fma(-r0, (double)inv_f, 2.0);
+            const double k = inv_r0d * args.inv_dr;
+            const float inv_r0 = (float)inv_r0d;
             const float e = args.dr * inv_r0;
             PulseParams p;
-            p.a = 2.0f * (float)wx * inv_r0 * inv_dr;
-            p.b = 2.0f * (float)wy * inv_r0 * inv_dr;
-            p.c = inv_r0 * inv_dr;
+            p.a = (float)(2.0 * wx * k);          // each coefficient rounded to float once
+            p.b = (float)(2.0 * wy * k);
+            p.c = (float)k;
             p.q0m = (float)(qg - o) - 0.5f;
             p.c1 = -0.125f * e;
             p.c2 = 0.0625f * e * e;

@@ -180,8 +180,10 @@ sar_status setup_bp(sar_plan p)
     a.x0 = g.x0;
     a.y0 = g.y0;
     a.z0 = g.z0;
-    a.dx = (float)g.dx;
-    a.dy = (float)g.dy;
+    a.dx = g.dx;
+    a.dy = g.dy;
+    a.dxf = (float)g.dx;
+    a.dyf = (float)g.dy;
     a.nx = g.nx;
     a.ny = g.ny;
     a.tiles_x = (g.nx + sar::kBpTileX - 1) / sar::kBpTileX;

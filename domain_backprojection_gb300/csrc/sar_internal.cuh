@@ -46,7 +46,8 @@ constexpr int kBpThreads = kBpTileX * kBpTileY / kBpRowsPerThread;   // 256
 struct BpArgs {
     // grid
     double x0, y0, z0;
-    float dx, dy;
+    double dx, dy;           // pixel spacing (float64: tile centres must not inherit float32 rounding)
+    float dxf, dyf;          // the same spacing in float32, for offsets inside a tile
     int nx, ny, tiles_x, tiles_y;
     // range axis
     double range_start;      // m
