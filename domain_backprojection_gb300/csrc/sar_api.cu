@@ -429,3 +429,65 @@ sar_status sar_plan_sync(sar_plan plan, void *stream)
 int32_t sar_plan_last_launches(sar_plan plan) { return plan ? plan->last_launches : 0; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// sar_form_image_noalloc: image formation whose compressed-line scratch is a
+// fixed array compiled into this library instead of caller- or plan-allocated
+// memory, for callers that cannot call cudaMalloc when they form an image
+// (memory fixed at start-up, or owned by an allocator the library cannot use).
+// The array costs every device that loads the library kNoallocScratchBytes
+// until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = (size_t)32 << 20;     // 32 MiB
+constexpr int kNoallocMaxDevices = 64;
+
+// In host code this name is only a stand-in for the symbol: its device address
+// comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) float2 g_noalloc_scratch[kNoallocScratchBytes / sizeof(float2)];
+
+std::mutex g_noalloc_mutex;
+float2 *g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+// Device address of the scratch array on `device`, which must be current.
+sar_status noalloc_scratch(int device, float2 **out)
+{
+    if (device < 0 || device >= kNoallocMaxDevices) return SAR_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[device]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return SAR_ERR_CUDA;
+        g_noalloc_ptr[device] = static_cast<float2 *>(p);
+    }
+    *out = g_noalloc_ptr[device];
+    return SAR_OK;
+}
+
+}  // namespace
+
+extern "C" sar_status sar_form_image_noalloc(sar_plan plan, const void *raw, const double *pos, void *image,
+                                             void *stream)
+{
+    if (!plan || !raw || !pos || !image) return SAR_ERR_INVALID_ARG;
+    if (!plan->has_grid) return SAR_ERR_UNSUPPORTED;
+    size_t need = 0;
+    sar_workspace_size(plan, &need);
+    if (need > kNoallocScratchBytes) return SAR_ERR_UNSUPPORTED;
+    if (!aligned16(raw) || !aligned16(image) || (reinterpret_cast<uintptr_t>(pos) & 7u)) return SAR_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    float2 *scratch = nullptr;
+    sar_status st = noalloc_scratch(plan->device, &scratch);
+    if (st != SAR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // every scratch element the backprojection reads is written by the range compression first,
+    // so nothing left by an earlier call needs clearing
+    plan->last_launches = 1;
+    st = cuda_status(sar::launch_rc(plan->rc, static_cast<const float2 *>(raw), scratch, plan->radar.n_pulses, s));
+    if (st != SAR_OK) return st;
+    return do_backproject(plan, scratch, pos, 0, plan->radar.n_pulses, image, 0, s);
+}

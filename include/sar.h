@@ -128,6 +128,22 @@ sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, voi
 sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double *pos_host, void *image_host,
                                void *stream);
 
+/* Image formation that allocates nothing (the pages have no counterpart: this
+ * is a deployment variant of sar_form_image).  For callers that cannot call
+ * cudaMalloc when they form an image -- processing loops whose device memory
+ * is fixed at start-up, or hosts whose device memory belongs to an allocator
+ * this library cannot use.  The compressed lines go to a 32 MiB array compiled
+ * into the library, which every device that loads the library holds until the
+ * process exits; the caller passes only inputs and outputs (raw, pos, image as
+ * in sar_form_image).  Plans whose Na * U * Nr * 8 bytes exceed 32 MiB get
+ * SAR_ERR_UNSUPPORTED before anything is launched.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress, once per device);
+ * make that first call before any stream capture.  All calls share the one
+ * array: calls whose work overlaps on the GPU (other streams, other plans)
+ * race on it and must be serialised by the caller.  Nothing in it needs
+ * clearing between calls. */
+sar_status sar_form_image_noalloc(sar_plan plan, const void *raw, const double *pos, void *image, void *stream);
+
 /* Synchronise `stream`, then read and clear the plan's device error flags:
  * SAR_ERR_INTERNAL if a bounds check fired, SAR_ERR_UNSUPPORTED if a geometry
  * validity check failed, SAR_ERR_CUDA on an asynchronous CUDA error. */
