@@ -51,29 +51,33 @@ def declared_symbols() -> list:
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(sar_\w+)\s*\(", text, re.M)))
 
 
+def load_library(path: str):
+    """Load a build of libsar.so at `path` and declare its entry points' signatures."""
+    L = ctypes.CDLL(path)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "sar_plan_create": ([P, P, ctypes.c_int, P], ctypes.c_int),
+        "sar_plan_destroy": ([P], ctypes.c_int),
+        "sar_workspace_size": ([P, P], ctypes.c_int),
+        "sar_range_compress": ([P, P, P, I64, P], ctypes.c_int),
+        "sar_backproject": ([P, P, P, I32, I32, P, ctypes.c_int, P], ctypes.c_int),
+        "sar_form_image": ([P, P, P, P, P, SZ, P], ctypes.c_int),
+        "sar_form_image_host": ([P, P, P, P, P], ctypes.c_int),
+        "sar_plan_sync": ([P, P], ctypes.c_int),
+        "sar_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "sar_plan_last_launches": ([P], I32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
-        L = ctypes.CDLL(path)
-        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
-        sig = {
-            "sar_plan_create": ([P, P, ctypes.c_int, P], ctypes.c_int),
-            "sar_plan_destroy": ([P], ctypes.c_int),
-            "sar_workspace_size": ([P, P], ctypes.c_int),
-            "sar_range_compress": ([P, P, P, I64, P], ctypes.c_int),
-            "sar_backproject": ([P, P, P, I32, I32, P, ctypes.c_int, P], ctypes.c_int),
-            "sar_form_image": ([P, P, P, P, P, SZ, P], ctypes.c_int),
-            "sar_form_image_host": ([P, P, P, P, P], ctypes.c_int),
-            "sar_plan_sync": ([P, P], ctypes.c_int),
-            "sar_status_string": ([ctypes.c_int], ctypes.c_char_p),
-            "sar_plan_last_launches": ([P], I32),
-        }
-        for name, (args, res) in sig.items():
-            fn = getattr(L, name)
-            fn.argtypes = args
-            fn.restype = res
-        _lib = L
+        _lib = load_library(_build.build())
     return _lib
 
 

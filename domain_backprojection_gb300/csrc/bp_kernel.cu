@@ -3,14 +3,18 @@
 // the linearly interpolated range-compressed echo at its range, multiplied by
 // exp(+j 4 pi fc R / c0).
 //
-// Work decomposition.  One CTA owns a 32 x 32 pixel tile (warps run along x,
-// the azimuth axis, so the 32 lanes of a warp read nearly the same range
-// samples); each thread keeps four pixels' complex sums in registers for the
-// whole pulse range.  The CTA walks the pulses in batches: for each pulse of a
-// batch it first evaluates, in float64, the range R0 from the antenna to the
-// tile centre, then stages the window of compressed samples the tile can touch
-// in shared memory (section 2.3 of the same page stages echo data per image
-// block the same way).
+// Work decomposition.  One CTA owns a 64 x 32 pixel tile, long in azimuth (x):
+// pixels that differ only in x lie at nearly the same range, so the window of
+// compressed samples a tile touches grows with its range (y) extent only and
+// staging it is shared by twice as many pixels.  Warps run along x, so the 32
+// lanes of a warp read nearly the same samples; each thread keeps four pixels'
+// complex sums in registers for the whole pulse range.  The CTA walks the
+// pulses in batches: for each pulse of a batch it first evaluates, in float64,
+// the range R0 from the antenna to the tile centre, then stages the window of
+// compressed samples the tile can touch in shared memory (section 2.3 of the
+// same page stages echo data per image block the same way).  Long pulse ranges
+// are split into slices (gridDim.z) whose partial images a second kernel adds
+// in slice order, so that small images and the last wave still fill the GPU.
 //
 // Range and phase precision.  At X band the phase 4 pi R / lambda needs R to
 // ~1e-5 m at R ~ 6 km, beyond float32 (the listing in section 3.3 computes the
@@ -37,11 +41,6 @@
 namespace sar {
 namespace {
 
-struct __align__(16) PulseParams {
-    float a, b, c, q0m;       // g_bins = a dx + b dy + c |d|^2 ; qm0 = frac(bin of R0) - 1/2
-    float c1, c2, c3, theta;  // series coefficients in bins; phase of the window origin (rad)
-};
-
 constexpr float kRoundMagic = 12582912.0f;                 // 1.5 * 2^23: x + magic rounds x to an integer
 constexpr unsigned kRoundMagicBits = 0x4B400000u;
 
@@ -52,26 +51,70 @@ __device__ __forceinline__ float4 lds128(unsigned addr)
     return v;
 }
 
+// One pulse's contribution to this thread's pixels (one column, kBpRowsPerThread rows).
 template <bool kCheck>
-__global__ void __launch_bounds__(kBpThreads, 3) bp_kernel(BpArgs args)
+__device__ __forceinline__ void pixel_pulse(const float4 pa, const float4 pc, const int4 wv, const unsigned base,
+                                            const float adx, const float *oy, const float *od2, float *acc_re,
+                                            float *acc_im, const BpArgs &args)
+{
+#pragma unroll
+    for (int k = 0; k < kBpRowsPerThread; k++) {
+        const float g = fmaf(pa.y, oy[k], fmaf(pa.z, od2[k], adx));
+        float t = fmaf(g, fmaf(g, pc.z, pc.y), pc.x);
+        t = fmaf(g, t, 0.5f);
+        const float qm = fmaf(g, t, pa.w);
+        const float rnd = __fadd_rn(qm, kRoundMagic);
+        const unsigned addr = base + (__float_as_uint(rnd) << 4);
+        if (kCheck) {
+            const int e = (int)(__float_as_uint(rnd) - kRoundMagicBits) + args.wh;
+            if (e < wv.y || e > wv.z) {
+                atomicOr(args.err, kDevErrBounds);
+                continue;
+            }
+        }
+        const float4 v = lds128(addr);
+        const float vr = fmaf(qm, v.z, v.x);
+        const float vi = fmaf(qm, v.w, v.y);
+        float sn, cs;
+        __sincosf(fmaf(qm, args.two_pi_kappa, pc.w), &sn, &cs);
+        acc_re[k] = fmaf(vr, cs, acc_re[k]);
+        acc_re[k] = fmaf(-vi, sn, acc_re[k]);
+        acc_im[k] = fmaf(vr, sn, acc_im[k]);
+        acc_im[k] = fmaf(vi, cs, acc_im[k]);
+    }
+}
+
+// Shared memory of one CTA: per pulse of the batch two float4 of parameters
+//   (a, b, c, q0m): g_bins = a dx + b dy + c |d|^2, qm0 = frac(bin of R0) - 1/2
+//   (c1, c2, c3, theta): series coefficients in bins, phase of the window origin (rad)
+// one int4 (origin o, first and last staged entry, unused), then the staged windows
+// [pulses_per_batch][w] of (tau.re, tau.im, sigma.re, sigma.im).
+template <bool kCheck>
+__global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
 {
     extern __shared__ float4 smem4[];
     const int pb_max = args.pulses_per_batch;
-    PulseParams *prm = reinterpret_cast<PulseParams *>(smem4);
-    int *origin = reinterpret_cast<int *>(prm + pb_max);
-    float4 *stage = smem4 + 2 * pb_max + (pb_max + 3) / 4;       // [pb_max][w] of (tau.re, tau.im, sigma.re, sigma.im)
+    float4 *prm = smem4;
+    int4 *win = reinterpret_cast<int4 *>(smem4 + 2 * pb_max);
+    float4 *stage = smem4 + 3 * pb_max;
     const int w = args.w, wh = args.wh;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int tile_x = blockIdx.x, tile_y = blockIdx.y;
+    constexpr int kRowWarps = kBpTileY / kBpRowsPerThread;          // warps per column group (8)
+    const int col = (warp / kRowWarps) * 32 + lane;                  // pixel column inside the tile
+    const int row0 = (warp % kRowWarps) * kBpRowsPerThread;          // first of this thread's rows
+    const int tile_x = blockIdx.x, tile_y = blockIdx.y, slice = blockIdx.z;
+    const int p_begin = args.pulse_begin + slice * args.slice_len;
+    const int p_end = min(args.pulse_end, p_begin + args.slice_len);
     // tile centre (float64) and this thread's pixel offsets from it (float32)
     const double cx = args.x0 + ((double)tile_x * kBpTileX + 0.5 * (kBpTileX - 1)) * args.dx;
     const double cy = args.y0 + ((double)tile_y * kBpTileY + 0.5 * (kBpTileY - 1)) * args.dy;
-    const float ox = ((float)lane - 0.5f * (kBpTileX - 1)) * args.dxf;
+    const float hx = 0.5f * (kBpTileX - 1) * args.dxf, hy = 0.5f * (kBpTileY - 1) * args.dyf;
+    const float ox = ((float)col - 0.5f * (kBpTileX - 1)) * args.dxf;
     float oy[kBpRowsPerThread], od2[kBpRowsPerThread];
 #pragma unroll
     for (int k = 0; k < kBpRowsPerThread; k++) {
-        const int ly = warp * kBpRowsPerThread + k;
+        const int ly = row0 + k;
         oy[k] = ((float)ly - 0.5f * (kBpTileY - 1)) * args.dyf;
         od2[k] = fmaf(ox, ox, oy[k] * oy[k]);
     }
@@ -79,12 +122,14 @@ __global__ void __launch_bounds__(kBpThreads, 3) bp_kernel(BpArgs args)
 #pragma unroll
     for (int k = 0; k < kBpRowsPerThread; k++) acc_re[k] = acc_im[k] = 0.0f;
 
-    const unsigned stage_base = (unsigned)__cvta_generic_to_shared(stage);
-    const int64_t ns = args.n_samples;
+    // entry e of pulse row p lives at stage_row0 + 16 (p w + e); the address of entry round(qm) + wh
+    // is formed from the bit pattern of qm + magic with 32-bit wrap-around
+    const unsigned stage_row0 = (unsigned)__cvta_generic_to_shared(stage) + 16u * (unsigned)wh - 16u * kRoundMagicBits;
+    const int ns = args.n_samples;
 
-    for (int n0 = args.pulse_begin; n0 < args.pulse_end; n0 += pb_max) {
-        const int pb = min(pb_max, args.pulse_end - n0);
-        // ---- per-(tile, pulse) reference range in float64
+    for (int n0 = p_begin; n0 < p_end; n0 += pb_max) {
+        const int pb = min(pb_max, p_end - n0);
+        // ---- per-(tile, pulse) reference range in float64, window extent in float32
         if (threadIdx.x < pb) {
             const int n = n0 + threadIdx.x;
             const double wx = cx - args.pos[3 * n + 0];
@@ -104,87 +149,104 @@ __global__ void __launch_bounds__(kBpThreads, 3) bp_kernel(BpArgs args)
             // 1 / (r0 dr) to float64 accuracy: float reciprocal refined by one Newton step
             const float inv_f = 1.0f / (float)r0;
             const double inv_r0d = (double)inv_f * fma(-r0, (double)inv_f, 2.0);
-            const double k = inv_r0d * args.inv_dr;
-            const float inv_r0 = (float)inv_r0d;
-            const float e = args.dr * inv_r0;
-            PulseParams p;
-            p.a = (float)(2.0 * wx * k);          // each coefficient rounded to float once
-            p.b = (float)(2.0 * wy * k);
-            p.c = (float)k;
-            p.q0m = (float)(qg - o) - 0.5f;
-            p.c1 = -0.125f * e;
-            p.c2 = 0.0625f * e * e;
-            p.c3 = -0.0390625f * e * e * e;
+            const double kk = inv_r0d * args.inv_dr;
+            const float e = args.dr * (float)inv_r0d;
+            float4 pa, pc;
+            pa.x = (float)(2.0 * wx * kk);          // each coefficient rounded to float once
+            pa.y = (float)(2.0 * wy * kk);
+            pa.z = (float)kk;
+            pa.w = (float)(qg - o) - 0.5f;
+            pc.x = -0.125f * e;
+            pc.y = 0.0625f * e * e;
+            pc.z = -0.0390625f * e * e * e;
             double t = fma(args.kappa, o + 0.5, args.phase0_turns);
             t -= rint(t);
-            p.theta = (float)(6.283185307179586 * t);
+            pc.w = (float)(6.283185307179586 * t);
+            // staged entries: the tile's nearest and farthest pixel ranges (float32 is ample here)
+            // bound every pixel's bin; two entries of margin on each side
+            const float wxf = (float)wx, wyf = (float)wy, wzf = (float)wz;
+            const float nx_ = wxf + fminf(fmaxf(-wxf, -hx), hx), ny_ = wyf + fminf(fmaxf(-wyf, -hy), hy);
+            const float fx = fabsf(wxf) + hx, fy = fabsf(wyf) + hy;
+            const float rmin = sqrtf(fmaf(nx_, nx_, fmaf(ny_, ny_, wzf * wzf)));
+            const float rmax = sqrtf(fmaf(fx, fx, fmaf(fy, fy, wzf * wzf)));
+            const float r0f = (float)r0, qc = (float)(qg - o), idr = (float)args.inv_dr;
+            int e_lo = (int)floorf(fmaf(rmin - r0f, idr, qc)) - 2 + wh;
+            int e_hi = (int)floorf(fmaf(rmax - r0f, idr, qc)) + 2 + wh;
+            e_lo = max(e_lo, 0);
+            e_hi = min(e_hi, w - 1);
             if (!ok) {
-                p.a = p.b = p.c = p.q0m = p.c1 = p.c2 = p.c3 = p.theta = 0.0f;
+                pa = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                pc = pa;
+                e_lo = e_hi = wh;
                 atomicOr(args.err, kDevErrGeometry);
             }
-            prm[threadIdx.x] = p;
-            origin[threadIdx.x] = (int)o;
+            prm[2 * threadIdx.x] = pa;
+            prm[2 * threadIdx.x + 1] = pc;
+            win[threadIdx.x] = make_int4((int)o, e_lo, e_hi, 0);
         }
         __syncthreads();
-        // ---- stage the windows: entry e <-> global bin origin + e - wh
+        // ---- stage the windows, one warp per pulse row: entry e <-> global bin o + e - wh holds
+        // (tau, sigma) of samples v_I, v_{I+1}.  Lane j of a row handles the aligned sample pair
+        // (a0 + 2j, a0 + 2j + 1) plus the next sample, which give two consecutive entries.
         for (int p = warp; p < pb; p += kBpThreads / 32) {
+            const int4 wv = win[p];
             const float2 *line = args.rc + (int64_t)(n0 + p) * ns;
-            const int64_t first = (int64_t)origin[p] - wh;
-            float4 *row = stage + p * w;
-            for (int e = lane; e < w; e += 32) {
-                const int64_t I = first + e;
-                const float2 v0 = (I >= 0 && I < ns) ? __ldg(line + I) : make_float2(0.0f, 0.0f);
-                const float2 v1 = (I + 1 >= 0 && I + 1 < ns) ? __ldg(line + I + 1) : make_float2(0.0f, 0.0f);
-                const float sr = v1.x - v0.x, si = v1.y - v0.y;
-                const float im = (float)(e - wh) - 0.5f;
-                row[e] = make_float4(fmaf(-im, sr, v0.x), fmaf(-im, si, v0.y), sr, si);
+            const int first = wv.x - wh + wv.y;                 // global bin of entry e_lo
+            const int count = wv.z - wv.y + 1;                  // entries to stage
+            const int a0 = first & ~1;                          // even, so the pair load is 16-byte aligned
+            const int off = first - a0;
+            const int npairs = (count + 1 + off) >> 1;
+            const bool inside = a0 >= 0 && a0 + 2 * npairs < ns;
+            float4 *row = stage + p * w + wv.y;
+            float im = (float)(wv.y - wh) - 0.5f + (float)(2 * lane - off);   // (entry - wh) - 1/2
+            for (int j = lane; j < npairs; j += 32, im += 64.0f) {
+                const int s = a0 + 2 * j;
+                float2 va, vb, vc;
+                if (inside) {
+                    const float4 ab = __ldg(reinterpret_cast<const float4 *>(line + s));
+                    va = make_float2(ab.x, ab.y);
+                    vb = make_float2(ab.z, ab.w);
+                    vc = __ldg(line + s + 2);
+                } else {
+                    const float2 z = make_float2(0.0f, 0.0f);
+                    va = (s >= 0 && s < ns) ? __ldg(line + s) : z;
+                    vb = (s + 1 >= 0 && s + 1 < ns) ? __ldg(line + s + 1) : z;
+                    vc = (s + 2 >= 0 && s + 2 < ns) ? __ldg(line + s + 2) : z;
+                }
+                const int c = 2 * j - off;                      // entry of the pair's first sample
+                if (c >= 0) {
+                    const float sr = vb.x - va.x, si = vb.y - va.y;
+                    row[c] = make_float4(fmaf(-im, sr, va.x), fmaf(-im, si, va.y), sr, si);
+                }
+                if (c + 1 < count) {
+                    const float sr = vc.x - vb.x, si = vc.y - vb.y, im1 = im + 1.0f;
+                    row[c + 1] = make_float4(fmaf(-im1, sr, vb.x), fmaf(-im1, si, vb.y), sr, si);
+                }
             }
         }
         __syncthreads();
         // ---- pixel x pulse inner loop
+#pragma unroll 2
         for (int p = 0; p < pb; p++) {
-            const PulseParams P = prm[p];
-            // address of entry round(qm) + wh, from the bit pattern of qm + magic (32-bit wrap-around)
-            const unsigned base = stage_base + (unsigned)(p * w) * 16u + 16u * (unsigned)wh - 16u * kRoundMagicBits;
-            const float adx = P.a * ox;
-#pragma unroll
-            for (int k = 0; k < kBpRowsPerThread; k++) {
-                const float g = fmaf(P.b, oy[k], fmaf(P.c, od2[k], adx));
-                float t = fmaf(g, P.c3, P.c2);
-                t = fmaf(g, t, P.c1);
-                t = fmaf(g, t, 0.5f);
-                const float qm = fmaf(g, t, P.q0m);
-                const float rnd = __fadd_rn(qm, kRoundMagic);
-                const unsigned addr = base + (__float_as_uint(rnd) << 4);
-                if (kCheck) {
-                    const int e = (int)(__float_as_uint(rnd) - kRoundMagicBits) + wh;
-                    if (e < 0 || e >= w) {
-                        atomicOr(args.err, kDevErrBounds);
-                        continue;
-                    }
-                }
-                const float4 v = lds128(addr);
-                const float vr = fmaf(qm, v.z, v.x);
-                const float vi = fmaf(qm, v.w, v.y);
-                float s, c;
-                __sincosf(fmaf(qm, args.two_pi_kappa, P.theta), &s, &c);
-                acc_re[k] = fmaf(vr, c, acc_re[k]);
-                acc_re[k] = fmaf(-vi, s, acc_re[k]);
-                acc_im[k] = fmaf(vr, s, acc_im[k]);
-                acc_im[k] = fmaf(vi, c, acc_im[k]);
-            }
+            const float4 pa = prm[2 * p], pc = prm[2 * p + 1];
+            const int4 wv = kCheck ? win[p] : make_int4(0, 0, 0, 0);
+            const unsigned base = stage_row0 + (unsigned)(p * w) * 16u;
+            const float adx = pa.x * ox;
+            pixel_pulse<kCheck>(pa, pc, wv, base, adx, oy, od2, acc_re, acc_im, args);
         }
         __syncthreads();
     }
-    // ---- store
-    const int ix = tile_x * kBpTileX + lane;
+    // ---- store: straight into the image with one slice, else into this slice's partial image
+    const int ix = tile_x * kBpTileX + col;
+    const bool direct = gridDim.z == 1;
+    float2 *out = direct ? args.image : args.partial + (int64_t)slice * args.nx * args.ny;
 #pragma unroll
     for (int k = 0; k < kBpRowsPerThread; k++) {
-        const int iy = tile_y * kBpTileY + warp * kBpRowsPerThread + k;
+        const int iy = tile_y * kBpTileY + row0 + k;
         if (ix < args.nx && iy < args.ny) {
-            float2 *dst = args.image + (int64_t)iy * args.nx + ix;
+            float2 *dst = out + (int64_t)iy * args.nx + ix;
             float2 v = make_float2(acc_re[k], acc_im[k]);
-            if (args.accumulate) {
+            if (direct && args.accumulate) {
                 const float2 old = *dst;
                 v.x += old.x;
                 v.y += old.y;
@@ -194,28 +256,56 @@ __global__ void __launch_bounds__(kBpThreads, 3) bp_kernel(BpArgs args)
     }
 }
 
+// image = (accumulate ? image : 0) + partial_0 + partial_1 + ... in slice order, so the result does
+// not depend on which slice finished first
+__global__ void bp_reduce_kernel(const float2 *__restrict__ partial, int slices, int64_t npix, float2 *image,
+                                 int accumulate)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < npix; i += (int64_t)gridDim.x * blockDim.x) {
+        float2 acc = accumulate ? image[i] : make_float2(0.0f, 0.0f);
+        for (int s = 0; s < slices; s++) {
+            const float2 v = __ldg(partial + s * npix + i);
+            acc.x += v.x;
+            acc.y += v.y;
+        }
+        image[i] = acc;
+    }
+}
+
 }  // namespace
 
 size_t bp_smem_bytes(int w, int pulses_per_batch)
 {
-    const int pb = pulses_per_batch;
-    return (size_t)(2 * pb + (pb + 3) / 4) * sizeof(float4) + (size_t)pb * w * sizeof(float4);
+    return (size_t)pulses_per_batch * (3 + (size_t)w) * sizeof(float4);
 }
 
-cudaError_t bp_configure()
+cudaError_t bp_configure(int smem_bytes)
 {
-    cudaError_t e = cudaFuncSetAttribute(bp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(bp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(bp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    return cudaFuncSetAttribute(bp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-cudaError_t launch_bp(const BpArgs &a, bool check_bounds, cudaStream_t s)
+int bp_ctas_per_sm(int smem_bytes)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bp_kernel<false>, kBpThreads, smem_bytes) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s)
 {
     if (a.pulse_end <= a.pulse_begin) return cudaSuccess;
-    const dim3 grid(a.tiles_x, a.tiles_y);
+    const dim3 grid(a.tiles_x, a.tiles_y, slices);
     const size_t smem = bp_smem_bytes(a.w, a.pulses_per_batch);
     if (check_bounds) bp_kernel<true><<<grid, kBpThreads, smem, s>>>(a);
     else bp_kernel<false><<<grid, kBpThreads, smem, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || slices == 1) return e;
+    const int64_t npix = (int64_t)a.nx * a.ny;
+    const int blocks = (int)((npix + 255) / 256 < 4096 ? (npix + 255) / 256 : 4096);
+    bp_reduce_kernel<<<blocks, 256, 0, s>>>(a.partial, slices, npix, a.image, a.accumulate);
     return cudaGetLastError();
 }
 

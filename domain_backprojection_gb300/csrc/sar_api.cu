@@ -20,6 +20,9 @@ struct sar_plan_s {
     float2 *d_tables = nullptr;       // H | tw | ptw_hi | ptw_lo in one allocation
     // backprojection
     sar::BpArgs bp{};
+    int bp_slots = 1;                 // CTAs of bp_kernel resident on the whole device at once
+    int bp_max_slices = 1;            // pulse slices the partial-image buffer can hold
+    float2 *d_partial = nullptr;      // [bp_max_slices][ny][nx] partial images
     // device error word and its pinned host mirror
     int *d_err = nullptr;
     int *h_err = nullptr;
@@ -172,6 +175,27 @@ sar_status setup_rc(sar_plan p)
     return cuda_status(sar::rc_configure(n));
 }
 
+// Pulse slices for a backprojection of `pulses` pulses: the tiles x slices work units should fill
+// the resident CTA slots in whole waves.  A larger count is taken only when it cuts the estimated
+// time (waves per unit of work) by at least 3%; each slice keeps at least 16 pulses.
+int bp_pick_slices(sar_plan p, int pulses)
+{
+    const long long tiles = (long long)p->bp.tiles_x * p->bp.tiles_y;
+    const long long slots = p->bp_slots > 0 ? p->bp_slots : 1;
+    int cap = pulses / 16;
+    if (cap > sar::kBpMaxSlices) cap = sar::kBpMaxSlices;
+    int best = 1;
+    double best_cost = (double)((tiles + slots - 1) / slots);
+    for (int sl = 2; sl <= cap; sl++) {
+        const double cost = (double)((tiles * sl + slots - 1) / slots) / sl;
+        if (cost < 0.97 * best_cost) {
+            best = sl;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
 sar_status setup_bp(sar_plan p)
 {
     const sar_radar &r = p->radar;
@@ -206,22 +230,39 @@ sar_status setup_bp(sar_plan p)
     a.wh = (int)std::ceil(rt / dr) + 3;
     a.w = 2 * a.wh + 1;
     a.min_range_tiles = (float)(100.0 * rt);
-    // pulses per batch: as many as fit 64 KB of staging (three CTAs per SM), between 4 and 32
-    int pb = (int)((64 * 1024) / ((size_t)a.w * sizeof(float4) + 36));
+    // pulses per batch: as many as fit 108 KB of staging (two CTAs per SM), between 4 and 32
+    int pb = (int)((108 * 1024) / (((size_t)a.w + 3) * sizeof(float4)));
     if (pb > 32) pb = 32;
     if (pb < 4) {
         pb = 4;
-        if (sar::bp_smem_bytes(a.w, pb) > 96 * 1024) return SAR_ERR_UNSUPPORTED;   // pixels too coarse for a tile
+        if (sar::bp_smem_bytes(a.w, pb) > 200 * 1024) return SAR_ERR_UNSUPPORTED;   // pixels too coarse for a tile
     }
     a.pulses_per_batch = pb;
     a.err = p->d_err;
-    return cuda_status(sar::bp_configure());
+    const int smem = (int)sar::bp_smem_bytes(a.w, pb);
+    cudaError_t e = sar::bp_configure(smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->bp_slots = sar::bp_ctas_per_sm(smem) * sms;
+    // partial images for the largest pulse slicing a full-aperture call can pick (at most 512 MB)
+    const size_t img_bytes = (size_t)g.nx * g.ny * sizeof(float2);
+    int smax = bp_pick_slices(p, r.n_pulses);
+    while (smax > 1 && (size_t)smax * img_bytes > ((size_t)512 << 20)) smax--;
+    p->bp_max_slices = smax;
+    if (smax > 1) {
+        e = cudaMalloc(&p->d_partial, (size_t)smax * img_bytes);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return SAR_OK;
 }
 
 void free_plan(sar_plan p)
 {
     if (!p) return;
     cudaFree(p->d_tables);
+    cudaFree(p->d_partial);
     cudaFree(p->d_err);
     if (p->h_err) cudaFreeHost(p->h_err);
     cudaFree(p->d_raw);
@@ -246,8 +287,12 @@ sar_status do_backproject(sar_plan plan, const void *rc, const double *pos, int3
     a.pulse_begin = pulse_begin;
     a.pulse_end = pulse_begin + pulse_count;
     a.accumulate = accumulate ? 1 : 0;
-    plan->last_launches += 1;
-    return cuda_status(sar::launch_bp(a, plan->check_bounds, s));
+    int slices = bp_pick_slices(plan, pulse_count);
+    if (slices > plan->bp_max_slices) slices = plan->bp_max_slices;
+    a.slice_len = (pulse_count + slices - 1) / slices;
+    a.partial = plan->d_partial;
+    plan->last_launches += slices > 1 ? 2 : 1;
+    return cuda_status(sar::launch_bp(a, slices, plan->check_bounds, s));
 }
 
 }  // namespace

@@ -38,10 +38,11 @@ cudaError_t rc_configure(int n);
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s);
 
 // ----------------------------------------------------------- backprojection
-constexpr int kBpTileX = 32;     // pixels per tile along x (one warp lane each)
-constexpr int kBpTileY = 32;     // pixels per tile along y
+constexpr int kBpTileX = 64;     // pixels per tile along x (azimuth): two warps' lanes
+constexpr int kBpTileY = 32;     // pixels per tile along y (ground range)
 constexpr int kBpRowsPerThread = 4;
-constexpr int kBpThreads = kBpTileX * kBpTileY / kBpRowsPerThread;   // 256
+constexpr int kBpThreads = kBpTileX * kBpTileY / kBpRowsPerThread;   // 512
+constexpr int kBpMaxSlices = 32;
 
 struct BpArgs {
     // grid
@@ -62,6 +63,10 @@ struct BpArgs {
     int wh, w;
     int pulses_per_batch;
     float min_range_tiles;   // geometry validity: range >= this (m) per tile
+    // pulse slicing: slice s of gridDim.z sums pulses [pulse_begin + s * slice_len, ...) into
+    // partial + s * nx * ny (or straight into image when there is one slice)
+    int slice_len;
+    float2 *partial;
     // data
     const float2 *rc;        // [Na][U Nr]
     const double *pos;       // [Na][3]
@@ -72,7 +77,8 @@ struct BpArgs {
 };
 
 size_t bp_smem_bytes(int w, int pulses_per_batch);
-cudaError_t bp_configure();
-cudaError_t launch_bp(const BpArgs &a, bool check_bounds, cudaStream_t s);
+cudaError_t bp_configure(int smem_bytes);
+int bp_ctas_per_sm(int smem_bytes);
+cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s);
 
 }  // namespace sar
