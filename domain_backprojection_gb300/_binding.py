@@ -19,6 +19,8 @@ from . import build as _build
 _lib = None
 
 SAR_OK = 0
+SAR_RC_NATURAL = 0
+SAR_RC_POLYPHASE = 1
 STATUS_NAMES = {0: "SAR_OK", 1: "SAR_ERR_INVALID_ARG", 2: "SAR_ERR_UNSUPPORTED", 3: "SAR_ERR_NO_MEMORY",
                 4: "SAR_ERR_CUDA", 5: "SAR_ERR_TIMEOUT", 6: "SAR_ERR_INTERNAL"}
 
@@ -66,6 +68,7 @@ def load_library(path: str):
         "sar_plan_sync": ([P, P], ctypes.c_int),
         "sar_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "sar_plan_last_launches": ([P], I32),
+        "sar_plan_set_rc_layout": ([P, ctypes.c_int], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -237,6 +240,12 @@ def sar_form_image_host(plan: Plan, raw: torch.Tensor, pos: torch.Tensor, image:
 
 def sar_plan_sync(plan: Plan, stream=None) -> None:
     _check(lib().sar_plan_sync(plan.handle, _stream(stream)), "sar_plan_sync")
+
+
+def sar_plan_set_rc_layout(plan: Plan, layout: int) -> None:
+    """SAR_RC_NATURAL (sample U m + u at U m + u) or SAR_RC_POLYPHASE (at u Nr + m)."""
+    _check(lib().sar_plan_set_rc_layout(plan.handle, int(layout)), "sar_plan_set_rc_layout")
+    plan.layout = int(layout)
 
 
 def sar_plan_last_launches(plan: Plan) -> int:

@@ -89,7 +89,7 @@ __device__ __forceinline__ void pixel_pulse(const float4 pa, const float4 pc, co
 //   (c1, c2, c3, theta): series coefficients in bins, phase of the window origin (rad)
 // one int4 (origin o, first and last staged entry, unused), then the staged windows
 // [pulses_per_batch][w] of (tau.re, tau.im, sigma.re, sigma.im).
-template <bool kCheck>
+template <bool kCheck, bool kPlanar>
 __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
 {
     extern __shared__ float4 smem4[];
@@ -188,6 +188,38 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
         // ---- stage the windows, one warp per pulse row: entry e <-> global bin o + e - wh holds
         // (tau, sigma) of samples v_I, v_{I+1}.  Lane j of a row handles the aligned sample pair
         // (a0 + 2j, a0 + 2j + 1) plus the next sample, which give two consecutive entries.
+        if (kPlanar) {
+            // polyphase planes: sample I at (I & u_mask) Nr + (I >> u_shift).  Each lane loads one sample;
+            // the next one comes from the neighbouring lane (the last lane loads its own).
+            for (int p = warp; p < pb; p += kBpThreads / 32) {
+                const int4 wv = win[p];
+                const float2 *line = args.rc + (int64_t)(n0 + p) * ns;
+                const int first = wv.x - wh + wv.y;
+                const int count = wv.z - wv.y + 1;
+                float4 *row = stage + p * w + wv.y;
+                const float im0 = (float)(wv.y - wh) - 0.5f;
+                for (int c0 = 0; c0 <= count; c0 += 32) {
+                    const int c = c0 + lane;
+                    const int I = first + c;
+                    float2 v0 = make_float2(0.0f, 0.0f), v1;
+                    if (c <= count && I >= 0 && I < ns)
+                        v0 = __ldg(line + (I & args.u_mask) * args.n_range + (I >> args.u_shift));
+                    v1.x = __shfl_down_sync(0xffffffffu, v0.x, 1);
+                    v1.y = __shfl_down_sync(0xffffffffu, v0.y, 1);
+                    if (lane == 31) {
+                        const int J = I + 1;
+                        v1 = (c < count && J >= 0 && J < ns)
+                                 ? __ldg(line + (J & args.u_mask) * args.n_range + (J >> args.u_shift))
+                                 : make_float2(0.0f, 0.0f);
+                    }
+                    if (c < count) {
+                        const float sr = v1.x - v0.x, si = v1.y - v0.y;
+                        const float im = im0 + (float)c;
+                        row[c] = make_float4(fmaf(-im, sr, v0.x), fmaf(-im, si, v0.y), sr, si);
+                    }
+                }
+            }
+        } else
         for (int p = warp; p < pb; p += kBpThreads / 32) {
             const int4 wv = win[p];
             const float2 *line = args.rc + (int64_t)(n0 + p) * ns;
@@ -281,15 +313,19 @@ size_t bp_smem_bytes(int w, int pulses_per_batch)
 
 cudaError_t bp_configure(int smem_bytes)
 {
-    cudaError_t e = cudaFuncSetAttribute(bp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(bp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    const void *fns[] = {(const void *)bp_kernel<false, false>, (const void *)bp_kernel<false, true>,
+                         (const void *)bp_kernel<true, false>, (const void *)bp_kernel<true, true>};
+    for (const void *f : fns) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 int bp_ctas_per_sm(int smem_bytes)
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bp_kernel<false>, kBpThreads, smem_bytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bp_kernel<false, true>, kBpThreads, smem_bytes) != cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
 }
@@ -299,8 +335,13 @@ cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream
     if (a.pulse_end <= a.pulse_begin) return cudaSuccess;
     const dim3 grid(a.tiles_x, a.tiles_y, slices);
     const size_t smem = bp_smem_bytes(a.w, a.pulses_per_batch);
-    if (check_bounds) bp_kernel<true><<<grid, kBpThreads, smem, s>>>(a);
-    else bp_kernel<false><<<grid, kBpThreads, smem, s>>>(a);
+    if (check_bounds) {
+        if (a.planar) bp_kernel<true, true><<<grid, kBpThreads, smem, s>>>(a);
+        else bp_kernel<true, false><<<grid, kBpThreads, smem, s>>>(a);
+    } else {
+        if (a.planar) bp_kernel<false, true><<<grid, kBpThreads, smem, s>>>(a);
+        else bp_kernel<false, false><<<grid, kBpThreads, smem, s>>>(a);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || slices == 1) return e;
     const int64_t npix = (int64_t)a.nx * a.ny;

@@ -238,6 +238,11 @@ __global__ void __launch_bounds__(512) rc_fused_kernel(const float2 *__restrict_
                     reinterpret_cast<float4 *>(out)[i] =
                         make_float4(v.x * args.inv_n, -v.y * args.inv_n, v.z * args.inv_n, -v.w * args.inv_n);
                 }
+            } else if (args.planar) {
+                for (int m = threadIdx.x; m < n; m += blockDim.x) {
+                    const float2 v = Z[m];
+                    out[(int64_t)u * n + m] = make_float2(v.x * args.inv_n, -v.y * args.inv_n);
+                }
             } else {
                 for (int m = threadIdx.x; m < n; m += blockDim.x) {
                     const float2 v = Z[m];
@@ -249,6 +254,153 @@ __global__ void __launch_bounds__(512) rc_fused_kernel(const float2 *__restrict_
     }
 }
 
+// ---------------------------------------------------------------------------
+// Register-resident transforms for power-of-two lines, Nr = 512 ... 8192.
+// Each of the Nr/16 threads holds 16 elements, element t + T p in slot p
+// (T = Nr/16).  A transform is radix-16 passes (the last one radix 2, 4 or 8
+// when log2 Nr is not a multiple of 4) in the same self-sorting Stockham
+// order as above; the first pass reads the thread's registers, the last pass
+// leaves its results in registers in the same t + T p layout, and the passes
+// in between exchange through one padded shared-memory buffer (one element of
+// padding per 16 keeps the strided reads free of bank conflicts).  So the
+// forward transform's output, the filter multiply and the inverse transforms'
+// inputs never touch shared memory, and each transform costs log16(Nr) - 1
+// exchanges.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int pad16(int i) { return i + (i >> 4); }
+
+// w^p for p = 0 .. R-1 from w^1, multiplying powers of two (depth log2 R)
+template <int R>
+__device__ __forceinline__ void twiddle_powers(float2 w1, float2 *w)
+{
+    w[0] = make_float2(1.0f, 0.0f);
+    w[1] = w1;
+#pragma unroll
+    for (int p = 2; p < R; p++) {
+        const int hb = 1 << (31 - __clz(p));
+        w[p] = (hb == p) ? cmul(w[p / 2], w[p / 2]) : cmul(w[hb], w[p - hb]);
+    }
+}
+
+// One pass of radix R after L elements have been combined (L > 1): every
+// thread loads its 16/R butterflies from the buffer, then (after a barrier)
+// writes them back transformed, or keeps them when kLast.
+template <int N, int R, int L, bool kLast>
+__device__ __forceinline__ void reg_pass(float2 (&x)[16], float2 *buf, const float2 *__restrict__ tw)
+{
+    constexpr int T = N / 16, SP = N / (L * R), NB = 16 / R;
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < NB; i++) {
+        const int b = t + T * i;
+        const int jp = b % SP, kp = b / SP;
+#pragma unroll
+        for (int p = 0; p < R; p++) x[i * R + p] = buf[pad16(kp * SP * R + jp + SP * p)];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < NB; i++) {
+        const int b = t + T * i;
+        const int jp = b % SP, kp = b / SP;
+        float2 w[R];
+        twiddle_powers<R>(__ldg(tw + SP * kp), w);
+#pragma unroll
+        for (int p = 1; p < R; p++) x[i * R + p] = cmul(x[i * R + p], w[p]);
+        Dft<R>::run(x + i * R);
+        if (!kLast) {
+#pragma unroll
+            for (int q = 0; q < R; q++) buf[pad16((kp + L * q) * SP + jp)] = x[i * R + q];
+        }
+    }
+    if (!kLast) __syncthreads();
+    if (kLast && NB > 1) {
+        // outputs (t + T i) + (N / R) q = t + T (i + NB q): move them to slot i + NB q
+        float2 y[16];
+#pragma unroll
+        for (int i = 0; i < NB; i++)
+#pragma unroll
+            for (int q = 0; q < R; q++) y[i + NB * q] = x[i * R + q];
+#pragma unroll
+        for (int p = 0; p < 16; p++) x[p] = y[p];
+    }
+}
+
+// Forward DFT of the line held as x[p] = element t + T p; result in the same layout.
+template <int N>
+__device__ __forceinline__ void reg_dft(float2 (&x)[16], float2 *buf, const float2 *__restrict__ tw)
+{
+    constexpr int T = N / 16;
+    const int t = threadIdx.x;
+    Dft<16>::run(x);                                            // pass 1: L = 1, no twiddles
+#pragma unroll
+    for (int q = 0; q < 16; q++) buf[pad16(q * T + t)] = x[q];
+    __syncthreads();
+    if constexpr (N == 512) {
+        reg_pass<N, 16, 16, false>(x, buf, tw);
+        reg_pass<N, 2, 256, true>(x, buf, tw);
+    } else if constexpr (N == 1024) {
+        reg_pass<N, 16, 16, false>(x, buf, tw);
+        reg_pass<N, 4, 256, true>(x, buf, tw);
+    } else if constexpr (N == 2048) {
+        reg_pass<N, 16, 16, false>(x, buf, tw);
+        reg_pass<N, 8, 256, true>(x, buf, tw);
+    } else if constexpr (N == 4096) {
+        reg_pass<N, 16, 16, false>(x, buf, tw);
+        reg_pass<N, 16, 256, true>(x, buf, tw);
+    } else {
+        static_assert(N == 8192, "unsupported line length");
+        reg_pass<N, 16, 16, false>(x, buf, tw);
+        reg_pass<N, 16, 256, false>(x, buf, tw);
+        reg_pass<N, 2, 4096, true>(x, buf, tw);
+    }
+    __syncthreads();                                            // the buffer is free for the next transform
+}
+
+template <int N>
+__global__ void __launch_bounds__(N / 16) rc_reg_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc,
+                                                        int64_t n_lines, RcArgs args)
+{
+    extern __shared__ float4 smem4[];
+    float2 *buf = reinterpret_cast<float2 *>(smem4);
+    constexpr int T = N / 16;
+    const int t = threadIdx.x;
+    const int U = args.u;
+    for (int64_t line = blockIdx.x; line < n_lines; line += gridDim.x) {
+        float2 x[16], y[16];
+        const float2 *src = raw + line * N;
+#pragma unroll
+        for (int p = 0; p < 16; p++) x[p] = __ldg(src + t + T * p);
+        reg_dft<N>(x, buf, args.tw);
+        // matched filter
+#pragma unroll
+        for (int p = 0; p < 16; p++) y[p] = cmul(x[p], __ldg(args.h + t + T * p));
+        float2 *out = rc + line * (int64_t)(U * N);
+        for (int u = 0; u < U; u++) {
+            // y = Y exp(+j 2 pi k_s u / (U N)); inverse transform by the conjugate identity
+#pragma unroll
+            for (int p = 0; p < 16; p++) x[p] = cconj(y[p]);
+            reg_dft<N>(x, buf, args.tw);
+            if (args.planar || U == 1) {
+                float2 *plane = out + (int64_t)u * N;
+#pragma unroll
+                for (int p = 0; p < 16; p++) plane[t + T * p] = make_float2(x[p].x * args.inv_n, -x[p].y * args.inv_n);
+            } else {
+#pragma unroll
+                for (int p = 0; p < 16; p++)
+                    out[(int64_t)U * (t + T * p) + u] = make_float2(x[p].x * args.inv_n, -x[p].y * args.inv_n);
+            }
+            if (u + 1 < U) {
+#pragma unroll
+                for (int p = 0; p < 16; p++) y[p] = cmul(y[p], __ldg(args.ramp + t + T * p));
+            }
+        }
+    }
+}
+
+template <int N>
+size_t rc_reg_smem() { return (size_t)(N + N / 16) * sizeof(float2); }
+
 }  // namespace
 
 int rc_block_threads(int n) { return n >= 4096 ? 512 : 256; }
@@ -258,15 +410,29 @@ size_t rc_smem_bytes(int n) { return (size_t)3 * n * sizeof(float2); }
 cudaError_t rc_configure(int)
 {
     // the largest supported line (8192 samples) sets the limit, so plans of any size can coexist
-    return cudaFuncSetAttribute(rc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rc_smem_bytes(8192));
+    cudaError_t e = cudaFuncSetAttribute(rc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)rc_smem_bytes(8192));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_reg_kernel<8192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rc_reg_smem<8192>());
+    return e;
 }
+
+bool rc_has_reg_path(int n) { return n == 512 || n == 1024 || n == 2048 || n == 4096 || n == 8192; }
 
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s)
 {
     if (n_lines <= 0) return cudaSuccess;
     const int64_t max_grid = 1 << 20;
     const unsigned grid = (unsigned)(n_lines < max_grid ? n_lines : max_grid);
-    rc_fused_kernel<<<grid, rc_block_threads(a.n), rc_smem_bytes(a.n), s>>>(raw, rc, n_lines, a);
+    switch (a.n) {
+    case 512: rc_reg_kernel<512><<<grid, 512 / 16, rc_reg_smem<512>(), s>>>(raw, rc, n_lines, a); break;
+    case 1024: rc_reg_kernel<1024><<<grid, 1024 / 16, rc_reg_smem<1024>(), s>>>(raw, rc, n_lines, a); break;
+    case 2048: rc_reg_kernel<2048><<<grid, 2048 / 16, rc_reg_smem<2048>(), s>>>(raw, rc, n_lines, a); break;
+    case 4096: rc_reg_kernel<4096><<<grid, 4096 / 16, rc_reg_smem<4096>(), s>>>(raw, rc, n_lines, a); break;
+    case 8192: rc_reg_kernel<8192><<<grid, 8192 / 16, rc_reg_smem<8192>(), s>>>(raw, rc, n_lines, a); break;
+    default: rc_fused_kernel<<<grid, rc_block_threads(a.n), rc_smem_bytes(a.n), s>>>(raw, rc, n_lines, a); break;
+    }
     return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ struct sar_plan_s {
     sar_grid grid{};
     bool has_grid = false;
     bool check_bounds = false;
+    int rc_layout = SAR_RC_NATURAL;
     // range compression
     sar::RcArgs rc{};
     float2 *d_tables = nullptr;       // H | tw | ptw_hi | ptw_lo in one allocation
@@ -164,6 +165,11 @@ sar_status setup_rc(sar_plan p)
         const double ang = -2.0 * M_PI * (double)t / un;
         host.push_back(make_float2((float)std::cos(ang), (float)std::sin(ang)));
     }
+    for (int k = 0; k < n; k++) {                               // then n: exp(+2 pi i k_s / (U N))
+        const int ks = (2 * k >= n) ? k - n : k;
+        const double ang = 2.0 * M_PI * (double)ks / un;
+        host.push_back(make_float2((float)std::cos(ang), (float)std::sin(ang)));
+    }
     cudaError_t e = cudaMalloc(&p->d_tables, host.size() * sizeof(float2));
     if (e != cudaSuccess) return cuda_status(e);
     e = cudaMemcpy(p->d_tables, host.data(), host.size() * sizeof(float2), cudaMemcpyHostToDevice);
@@ -172,6 +178,8 @@ sar_status setup_rc(sar_plan p)
     a.tw = p->d_tables + n;
     a.ptw_hi = p->d_tables + 2 * n;
     a.ptw_lo = p->d_tables + 2 * n + n_hi;
+    a.ramp = p->d_tables + 2 * n + n_hi + n_lo;
+    a.planar = 0;
     return cuda_status(sar::rc_configure(n));
 }
 
@@ -218,6 +226,10 @@ sar_status setup_bp(sar_plan p)
     a.inv_dr = 1.0 / dr;
     a.dr = (float)dr;
     a.n_samples = r.n_range * r.upsample;
+    a.n_range = r.n_range;
+    a.u_shift = r.upsample == 8 ? 3 : r.upsample == 4 ? 2 : r.upsample == 2 ? 1 : 0;
+    a.u_mask = r.upsample - 1;
+    a.planar = 0;
     const double lambda = kC0 / r.fc;
     const double ph = 2.0 * r.range_start / lambda;
     a.phase0_turns = ph - std::floor(ph);
@@ -273,7 +285,7 @@ void free_plan(sar_plan p)
 }
 
 sar_status do_backproject(sar_plan plan, const void *rc, const double *pos, int32_t pulse_begin,
-                          int32_t pulse_count, void *image, int accumulate, cudaStream_t s)
+                          int32_t pulse_count, void *image, int accumulate, cudaStream_t s, int layout)
 {
     const size_t img_bytes = (size_t)plan->grid.nx * plan->grid.ny * sizeof(float2);
     if (pulse_count == 0) {
@@ -291,6 +303,7 @@ sar_status do_backproject(sar_plan plan, const void *rc, const double *pos, int3
     if (slices > plan->bp_max_slices) slices = plan->bp_max_slices;
     a.slice_len = (pulse_count + slices - 1) / slices;
     a.partial = plan->d_partial;
+    a.planar = (layout == SAR_RC_POLYPHASE && plan->radar.upsample > 1) ? 1 : 0;
     plan->last_launches += slices > 1 ? 2 : 1;
     return cuda_status(sar::launch_bp(a, slices, plan->check_bounds, s));
 }
@@ -381,7 +394,9 @@ sar_status sar_range_compress(sar_plan plan, const void *raw, void *rc, int64_t 
     DeviceGuard guard(plan->device);
     if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
     plan->last_launches = 1;
-    return cuda_status(sar::launch_rc(plan->rc, static_cast<const float2 *>(raw), static_cast<float2 *>(rc), n_lines,
+    sar::RcArgs a = plan->rc;
+    a.planar = plan->rc_layout == SAR_RC_POLYPHASE ? 1 : 0;
+    return cuda_status(sar::launch_rc(a, static_cast<const float2 *>(raw), static_cast<float2 *>(rc), n_lines,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -397,7 +412,7 @@ sar_status sar_backproject(sar_plan plan, const void *rc, const double *pos, int
     if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
     plan->last_launches = 0;
     return do_backproject(plan, rc, pos, pulse_begin, pulse_count, image, accumulate,
-                          static_cast<cudaStream_t>(stream));
+                          static_cast<cudaStream_t>(stream), plan->rc_layout);
 }
 
 sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, void *image, void *workspace,
@@ -414,10 +429,12 @@ sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, voi
     if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     plan->last_launches = 1;
-    sar_status st = cuda_status(sar::launch_rc(plan->rc, static_cast<const float2 *>(raw),
+    sar::RcArgs ra = plan->rc;
+    ra.planar = 1;
+    sar_status st = cuda_status(sar::launch_rc(ra, static_cast<const float2 *>(raw),
                                                static_cast<float2 *>(workspace), plan->radar.n_pulses, s));
     if (st != SAR_OK) return st;
-    return do_backproject(plan, workspace, pos, 0, plan->radar.n_pulses, image, 0, s);
+    return do_backproject(plan, workspace, pos, 0, plan->radar.n_pulses, image, 0, s, SAR_RC_POLYPHASE);
 }
 
 sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double *pos_host, void *image_host,
@@ -472,6 +489,13 @@ sar_status sar_plan_sync(sar_plan plan, void *stream)
 }
 
 int32_t sar_plan_last_launches(sar_plan plan) { return plan ? plan->last_launches : 0; }
+
+sar_status sar_plan_set_rc_layout(sar_plan plan, sar_rc_layout layout)
+{
+    if (!plan || (layout != SAR_RC_NATURAL && layout != SAR_RC_POLYPHASE)) return SAR_ERR_INVALID_ARG;
+    plan->rc_layout = layout;
+    return SAR_OK;
+}
 
 }  // extern "C"
 
@@ -532,7 +556,9 @@ extern "C" sar_status sar_form_image_noalloc(sar_plan plan, const void *raw, con
     // every scratch element the backprojection reads is written by the range compression first,
     // so nothing left by an earlier call needs clearing
     plan->last_launches = 1;
-    st = cuda_status(sar::launch_rc(plan->rc, static_cast<const float2 *>(raw), scratch, plan->radar.n_pulses, s));
+    sar::RcArgs ra = plan->rc;
+    ra.planar = 1;
+    st = cuda_status(sar::launch_rc(ra, static_cast<const float2 *>(raw), scratch, plan->radar.n_pulses, s));
     if (st != SAR_OK) return st;
-    return do_backproject(plan, scratch, pos, 0, plan->radar.n_pulses, image, 0, s);
+    return do_backproject(plan, scratch, pos, 0, plan->radar.n_pulses, image, 0, s, SAR_RC_POLYPHASE);
 }

@@ -30,9 +30,12 @@ struct RcArgs {
     const float2 *tw;        // w_N^t = exp(-2 pi i t / Nr), t in [0, Nr)
     const float2 *ptw_hi;    // exp(-2 pi i (hi << bits) / (U Nr))
     const float2 *ptw_lo;    // exp(-2 pi i lo / (U Nr)), lo < 2^bits
+    const float2 *ramp;      // exp(+2 pi i k_s / (U Nr)) for k in [0, Nr), k_s the signed frequency
+    int planar;              // output layout: 0 natural (sample U m + u at U m + u), 1 planes (at u Nr + m)
 };
 
 int rc_block_threads(int n);
+bool rc_has_reg_path(int n);
 size_t rc_smem_bytes(int n);
 cudaError_t rc_configure(int n);
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s);
@@ -68,7 +71,8 @@ struct BpArgs {
     int slice_len;
     float2 *partial;
     // data
-    const float2 *rc;        // [Na][U Nr]
+    const float2 *rc;        // [Na][U Nr], natural order or polyphase planes (planar != 0)
+    int planar, u_shift, u_mask, n_range;   // planes: sample I of a line at (I & u_mask) Nr + (I >> u_shift)
     const double *pos;       // [Na][3]
     float2 *image;           // [ny][nx]
     int pulse_begin, pulse_end;

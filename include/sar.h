@@ -128,6 +128,19 @@ sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, voi
 sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double *pos_host, void *image_host,
                                void *stream);
 
+/* Layout of compressed lines with U > 1, for sar_range_compress's output and
+ * sar_backproject's input.  SAR_RC_NATURAL (the default): sample j = U m + u of
+ * a line at index j.  SAR_RC_POLYPHASE: at index u Nr + m, i.e. U contiguous
+ * planes of Nr samples, plane u holding the samples with j mod U = u -- each
+ * of the U inverse transforms of range compression then writes one contiguous
+ * plane, which halves the kernel's memory traffic compared with interleaved
+ * stores.  The two layouts coincide for U = 1.  sar_form_image uses the
+ * polyphase layout for its workspace regardless of this setting. */
+typedef enum { SAR_RC_NATURAL = 0, SAR_RC_POLYPHASE = 1 } sar_rc_layout;
+
+/* Set the plan's compressed-line layout (SAR_ERR_INVALID_ARG for other values). */
+sar_status sar_plan_set_rc_layout(sar_plan plan, sar_rc_layout layout);
+
 /* Image formation that allocates nothing (the pages have no counterpart: this
  * is a deployment variant of sar_form_image).  For callers that cannot call
  * cudaMalloc when they form an image -- processing loops whose device memory

@@ -182,3 +182,22 @@ def test_form_image_host_matches_device_path():
     host = sar.sar_form_image_host(plan, raw_h, pos_h)
     torch.cuda.synchronize()
     assert torch.equal(host, dev.cpu())
+
+
+def test_polyphase_layout_backprojection_matches_natural():
+    # the same compressed lines in either layout give the same image
+    s = _small_case(70, 45, na=64)
+    plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
+    nat = sar.sar_range_compress(plan, s["raw"])
+    img_nat = sar.sar_backproject(plan, nat, s["pos"])
+    sar.sar_plan_set_rc_layout(plan, sar.SAR_RC_POLYPHASE)
+    pla = sar.sar_range_compress(plan, s["raw"])
+    img_pla = sar.sar_backproject(plan, pla, s["pos"])
+    sar.sar_plan_sync(plan)
+    U, n = s["radar"].upsample, s["radar"].n_range
+    assert torch.equal(pla.reshape(-1, U, n), nat.reshape(-1, n, U).transpose(1, 2))
+    assert torch.equal(img_nat, img_pla)
+    ref = oracle.backproject(s["radar"], s["grid"], nat.cpu().numpy(), s["pos"].cpu().numpy())
+    assert rel_l2(img_pla.cpu().numpy(), ref) <= IMG_TOL
+    L = sar.lib()
+    assert L.sar_plan_set_rc_layout(plan.handle, 7) == 1

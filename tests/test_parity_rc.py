@@ -98,3 +98,20 @@ def test_rc_subset_of_lines_and_bad_arguments():
                                 1, None) == 1
     assert L.sar_range_compress(plan.handle, ctypes.c_void_p(full.data_ptr()), ctypes.c_void_p(full.data_ptr()), 1,
                                 None) == 1
+
+
+@pytest.mark.parametrize("n,U", [(4096, 8), (2048, 4), (8192, 2), (6000, 8), (1000, 2), (512, 8)])
+def test_rc_polyphase_layout(n, U):
+    # plane u of a polyphase line holds the natural samples U m + u
+    radar = synth.Radar(range_start=5000.0, n_pulses=5, n_range=n, upsample=U)
+    raw = _noise(5, n, 17 * n + U)
+    plan = sar.sar_plan_create(radar, None, 0)
+    nat = sar.sar_range_compress(plan, raw.cuda())
+    sar.sar_plan_set_rc_layout(plan, sar.SAR_RC_POLYPHASE)
+    pla = sar.sar_range_compress(plan, raw.cuda())
+    sar.sar_plan_sync(plan)
+    pla = pla.cpu().numpy().reshape(5, U, n)
+    nat = nat.cpu().numpy().reshape(5, n, U).transpose(0, 2, 1)
+    assert np.array_equal(pla, nat)
+    ref = oracle.range_compress(radar, raw.numpy(), threads=ORACLE_THREADS).reshape(5, n, U).transpose(0, 2, 1)
+    assert rel_l2(pla, ref) <= RC_TOL
