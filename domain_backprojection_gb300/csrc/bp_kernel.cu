@@ -51,53 +51,253 @@ __device__ __forceinline__ float4 lds128(unsigned addr)
     return v;
 }
 
-// One pulse's contribution to this thread's pixels (one column, kBpRowsPerThread rows).
-template <bool kCheck>
-__device__ __forceinline__ void pixel_pulse(const float4 pa, const float4 pc, const int4 wv, const unsigned base,
-                                            const float adx, const float *oy, const float *od2, float *acc_re,
-                                            float *acc_im, const BpArgs &args)
+__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+
+// entry address = base + 16 * bits, one integer multiply-add (32-bit wrap-around)
+__device__ __forceinline__ unsigned entry_addr(unsigned base, float rnd)
 {
+    unsigned a;
+    asm("mad.lo.u32 %0, %1, 16, %2;" : "=r"(a) : "r"(__float_as_uint(rnd)), "r"(base));
+    return a;
+}
+
+// One pulse's contribution to this thread's pixels, two pixel rows at a time: every per-pixel
+// quantity of rows (2j, 2j + 1) is a register pair, so the range offset, the series, the rounding,
+// the phase argument and the complex multiply-accumulate each take one paired (FFMA2 / FADD2)
+// instruction for both pixels.  q4 points at the pulse's parameters, each duplicated into a pair:
+//   (a, a, b, b), (c, c, q0m, q0m), (c1, c1, c2, c2), (c3, c3, theta, theta).
+template <bool kCheck>
+__device__ __forceinline__ void pixel_pulse(const float4 *q4, const int4 wv, const unsigned base, const float2 ox2,
+                                            const float2 *oyp, const float2 *odp, float2 *acc_r, float2 *acc_i,
+                                            const BpArgs &args)
+{
+    const float4 Q0 = q4[0], Q1 = q4[1], Q2 = q4[2], Q3 = q4[3];
+    const float2 A2 = f2(Q0.x, Q0.y), B2 = f2(Q0.z, Q0.w), C2 = f2(Q1.x, Q1.y), QM2 = f2(Q1.z, Q1.w);
+    const float2 S1 = f2(Q2.x, Q2.y), S2 = f2(Q2.z, Q2.w), S3 = f2(Q3.x, Q3.y), TH = f2(Q3.z, Q3.w);
+    const float2 half2 = f2(0.5f, 0.5f), magic2 = f2(kRoundMagic, kRoundMagic);
+    const float2 tpk2 = f2(args.two_pi_kappa, args.two_pi_kappa);
+    const float2 adx2 = __fmul2_rn(A2, ox2);
 #pragma unroll
-    for (int k = 0; k < kBpRowsPerThread; k++) {
-        const float g = fmaf(pa.y, oy[k], fmaf(pa.z, od2[k], adx));
-        float t = fmaf(g, fmaf(g, pc.z, pc.y), pc.x);
-        t = fmaf(g, t, 0.5f);
-        const float qm = fmaf(g, t, pa.w);
-        const float rnd = __fadd_rn(qm, kRoundMagic);
-        const unsigned addr = base + (__float_as_uint(rnd) << 4);
+    for (int j = 0; j < kBpRowsPerThread / 2; j++) {
+        const float2 g = __ffma2_rn(B2, oyp[j], __ffma2_rn(C2, odp[j], adx2));
+        float2 t = __ffma2_rn(g, __ffma2_rn(g, S3, S2), S1);
+        t = __ffma2_rn(g, t, half2);
+        const float2 qm = __ffma2_rn(g, t, QM2);
+        const float2 rnd = __fadd2_rn(qm, magic2);
+        const float2 ph = __ffma2_rn(qm, tpk2, TH);
         if (kCheck) {
-            const int e = (int)(__float_as_uint(rnd) - kRoundMagicBits) + args.wh;
-            if (e < wv.y || e > wv.z) {
+            const int e0 = (int)(__float_as_uint(rnd.x) - kRoundMagicBits) + args.wh;
+            const int e1 = (int)(__float_as_uint(rnd.y) - kRoundMagicBits) + args.wh;
+            if (e0 < wv.y || e0 > wv.z || e1 < wv.y || e1 > wv.z) {
                 atomicOr(args.err, kDevErrBounds);
                 continue;
             }
         }
-        const float4 v = lds128(addr);
-        const float vr = fmaf(qm, v.z, v.x);
-        const float vi = fmaf(qm, v.w, v.y);
-        float sn, cs;
-        __sincosf(fmaf(qm, args.two_pi_kappa, pc.w), &sn, &cs);
-        acc_re[k] = fmaf(vr, cs, acc_re[k]);
-        acc_re[k] = fmaf(-vi, sn, acc_re[k]);
-        acc_im[k] = fmaf(vr, sn, acc_im[k]);
-        acc_im[k] = fmaf(vi, cs, acc_im[k]);
+        const float4 v0 = lds128(entry_addr(base, rnd.x));
+        const float4 v1 = lds128(entry_addr(base, rnd.y));
+        const float2 vr = f2(fmaf(qm.x, v0.z, v0.x), fmaf(qm.y, v1.z, v1.x));
+        const float2 vi = f2(fmaf(qm.x, v0.w, v0.y), fmaf(qm.y, v1.w, v1.y));
+        float2 sn, cs;
+        __sincosf(ph.x, &sn.x, &cs.x);
+        __sincosf(ph.y, &sn.y, &cs.y);
+        acc_r[j] = __ffma2_rn(vr, cs, acc_r[j]);
+        acc_r[j] = __ffma2_rn(f2(-vi.x, -vi.y), sn, acc_r[j]);
+        acc_i[j] = __ffma2_rn(vr, sn, acc_i[j]);
+        acc_i[j] = __ffma2_rn(vi, cs, acc_i[j]);
     }
 }
 
-// Shared memory of one CTA: per pulse of the batch two float4 of parameters
-//   (a, b, c, q0m): g_bins = a dx + b dy + c |d|^2, qm0 = frac(bin of R0) - 1/2
-//   (c1, c2, c3, theta): series coefficients in bins, phase of the window origin (rad)
-// one int4 (origin o, first and last staged entry, unused), then the staged windows
-// [pulses_per_batch][w] of (tau.re, tau.im, sigma.re, sigma.im).
+// ---------------------------------------------------------------------------
+// Double-float arithmetic: a value is an unevaluated sum hi + lo of two floats
+// with |lo| <= ulp(hi) / 2 (about 48 significant bits).  Error-free
+// transformations: Knuth's two-sum, Dekker's fast two-sum (|a| >= |b|) and the
+// FMA two-product.  Used for the per-(tile, pulse) reference range, whose phase
+// needs ~1e-7 m at ~10 km; float64 runs at a small fraction of the float32 rate
+// on this GPU, so the prep stays on the float32 pipe.
+// ---------------------------------------------------------------------------
+struct dflt {
+    float hi, lo;
+};
+__device__ __forceinline__ dflt df_fast(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    return {s, __fadd_rn(b, -__fadd_rn(s, -a))};
+}
+__device__ __forceinline__ dflt df_two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    const float bb = __fadd_rn(s, -a);
+    return {s, __fadd_rn(__fadd_rn(a, -__fadd_rn(s, -bb)), __fadd_rn(b, -bb))};
+}
+__device__ __forceinline__ dflt df_add(dflt x, dflt y)
+{
+    const dflt s = df_two_sum(x.hi, y.hi);
+    return df_fast(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+__device__ __forceinline__ dflt df_neg(dflt x) { return {-x.hi, -x.lo}; }
+__device__ __forceinline__ dflt df_mul(dflt x, dflt y)
+{
+    const float p = __fmul_rn(x.hi, y.hi);
+    float e = __fmaf_rn(x.hi, y.hi, -p);
+    e = __fmaf_rn(x.hi, y.lo, e);
+    e = __fmaf_rn(x.lo, y.hi, e);
+    return df_fast(p, e);
+}
+__device__ __forceinline__ dflt df_mulf(dflt x, float y)
+{
+    const float p = __fmul_rn(x.hi, y);
+    return df_fast(p, __fmaf_rn(x.lo, y, __fmaf_rn(x.hi, y, -p)));
+}
+// square root: correctly rounded float root refined by one Newton step in double-float
+__device__ __forceinline__ dflt df_sqrt(dflt x)
+{
+    const float s = __fsqrt_rn(x.hi);
+    const float p = __fmul_rn(s, s);
+    const float r = __fadd_rn(__fadd_rn(__fadd_rn(x.hi, -p), -__fmaf_rn(s, s, -p)), x.lo);
+    return df_fast(s, __fmul_rn(r, __fdiv_rn(0.5f, s)));
+}
+// reciprocal: correctly rounded float reciprocal refined by one Newton step
+__device__ __forceinline__ dflt df_rcp(dflt x)
+{
+    const float y = __frcp_rn(x.hi);
+    const dflt e = df_add({1.0f, 0.0f}, df_neg(df_mulf(x, y)));     // 1 - x y
+    return df_fast(y, __fmul_rn(y, e.hi));
+}
+// floor and fraction of a double-float whose hi part is below 2^23
+__device__ __forceinline__ float df_floor(dflt x, float &frac)
+{
+    float fl = floorf(x.hi);
+    float fr = __fadd_rn(__fadd_rn(x.hi, -fl), x.lo);                 // x.hi - fl is exact
+    if (fr < 0.0f) {
+        fl -= 1.0f;
+        fr += 1.0f;
+    } else if (fr >= 1.0f) {
+        fl += 1.0f;
+        fr -= 1.0f;
+    }
+    frac = fr;
+    return fl;
+}
+
+// Antenna positions, float64 [n][3] -> double-float [n][3] (hi, lo) pairs.
+__global__ void __launch_bounds__(256) bp_split_pos_kernel(const double *pos, float2 *out, int begin, int end)
+{
+    const int n = begin + blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= end) return;
+#pragma unroll
+    for (int k = 0; k < 3; k++) {
+        const double v = pos[3 * n + k];
+        const float hi = (float)v;
+        out[3 * n + k] = make_float2(hi, (float)(v - (double)hi));
+    }
+}
+
+// Per (tile, pulse) reference range (double-float) and window extent (float32), one thread each.
+// Output: pa = (a, b, c, q0m), pc = (c1, c2, c3, theta), win = (origin o, first entry, last entry, 0).
+__device__ __forceinline__ void tile_pulse_params(const BpArgs &args, int tile_x, int tile_y, int n, float4 &pa,
+                                                  float4 &pc, int4 &win)
+{
+    const int w = args.w, wh = args.wh;
+    const float2 *ap = args.pos_split + 3 * n;
+    const dflt ax = {ap[0].x, ap[0].y}, ay = {ap[1].x, ap[1].y}, az = {ap[2].x, ap[2].y};
+    // tile centre: x0 + (tile * 64 + 31.5) dx, y0 + (tile * 32 + 15.5) dy (the float multipliers are exact)
+    const dflt cx = df_add({args.x0s.x, args.x0s.y},
+                           df_mulf({args.dxs.x, args.dxs.y}, (float)tile_x * kBpTileX + 0.5f * (kBpTileX - 1)));
+    const dflt cy = df_add({args.y0s.x, args.y0s.y},
+                           df_mulf({args.dys.x, args.dys.y}, (float)tile_y * kBpTileY + 0.5f * (kBpTileY - 1)));
+    const float hx = 0.5f * (kBpTileX - 1) * args.dxf, hy = 0.5f * (kBpTileY - 1) * args.dyf;
+    const dflt wx = df_add(cx, df_neg(ax)), wy = df_add(cy, df_neg(ay)), wz = df_add({args.z0s.x, args.z0s.y}, df_neg(az));
+    const dflt r2 = df_add(df_mul(wx, wx), df_add(df_mul(wy, wy), df_mul(wz, wz)));
+    const dflt r0 = df_sqrt(r2);
+    // fractional global bin of the centre
+    const dflt qg = df_mul(df_add(r0, df_neg({args.rss.x, args.rss.y})), {args.idrs.x, args.idrs.y});
+    // Validity: finite, far enough for the range expansion (which bounds every pixel's offset
+    // inside the staged window), and a representable window origin.  Otherwise flag the plan
+    // and zero this pulse's parameters: every pixel then reads entry wh, inside the window.
+    const bool ok = (r0.hi >= args.min_range_tiles) && (fabsf(qg.hi) < 4.0e6f);
+    float qfrac = 0.0f;
+    const float o = ok ? df_floor(qg, qfrac) : 0.0f;
+    // coefficients of the range offset in bins: a = 2 wx / (r0 dr), b = 2 wy / (r0 dr), c = 1 / (r0 dr)
+    const dflt k = df_mul(df_rcp(r0), {args.idrs.x, args.idrs.y});
+    const float e = args.dr * __frcp_rn(r0.hi);
+    pa.x = 2.0f * df_mul(wx, k).hi;
+    pa.y = 2.0f * df_mul(wy, k).hi;
+    pa.z = k.hi;
+    pa.w = qfrac - 0.5f;
+    pc.x = -0.125f * e;
+    pc.y = 0.0625f * e * e;
+    pc.z = -0.0390625f * e * e * e;
+    // phase of the window origin (o + 1/2): frac((2/lambda) R_start + kappa (o + 1/2)) turns
+    float tfrac;
+    df_floor(df_add({args.ph0s.x, args.ph0s.y}, df_mulf({args.kps.x, args.kps.y}, o + 0.5f)), tfrac);
+    if (tfrac >= 0.5f) tfrac -= 1.0f;
+    pc.w = 6.28318530717958648f * tfrac;
+    // staged entries: the tile's nearest and farthest pixel ranges (float32 is ample here)
+    // bound every pixel's bin; two entries of margin on each side
+    const float wxf = wx.hi, wyf = wy.hi, wzf = wz.hi;
+    const float nx_ = wxf + fminf(fmaxf(-wxf, -hx), hx), ny_ = wyf + fminf(fmaxf(-wyf, -hy), hy);
+    const float fx = fabsf(wxf) + hx, fy = fabsf(wyf) + hy;
+    const float rmin = sqrtf(fmaf(nx_, nx_, fmaf(ny_, ny_, wzf * wzf)));
+    const float rmax = sqrtf(fmaf(fx, fx, fmaf(fy, fy, wzf * wzf)));
+    const float r0f = r0.hi, idr = args.idrs.x;
+    int e_lo = (int)floorf(fmaf(rmin - r0f, idr, qfrac)) - 2 + wh;
+    int e_hi = (int)floorf(fmaf(rmax - r0f, idr, qfrac)) + 2 + wh;
+    e_lo = max(e_lo, 0);
+    e_hi = min(e_hi, w - 1);
+    if (!ok) {
+        pa = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        pc = pa;
+        e_lo = e_hi = wh;
+        atomicOr(args.err, kDevErrGeometry);
+    }
+    win = make_int4((int)o, e_lo, e_hi, 0);
+}
+
+// The parameter table: entry (tile, pulse) at table + 3 (tile_index * pulse_count + pulse - pulse_begin).
+__global__ void __launch_bounds__(256) bp_prep_kernel(BpArgs args)
+{
+    const int64_t npulses = args.pulse_end - args.pulse_begin;
+    const int64_t total = npulses * args.tiles_x * args.tiles_y;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = i / npulses;
+        const int n = args.pulse_begin + (int)(i - tile * npulses);
+        float4 pa, pc;
+        int4 win;
+        tile_pulse_params(args, (int)(tile % args.tiles_x), (int)(tile / args.tiles_x), n, pa, pc, win);
+        float4 *dst = args.table + 3 * i;
+        dst[0] = pa;
+        dst[1] = pc;
+        dst[2] = make_float4(__int_as_float(win.x), __int_as_float(win.y), __int_as_float(win.z), 0.0f);
+    }
+}
+
+__device__ __forceinline__ void cp_async8(unsigned dst, const void *src, int src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Shared memory of one CTA:
+//   params [3][pulses_per_batch][4] float4 parameter quads (see pixel_pulse) and
+//          [3][pulses_per_batch] int4 windows (origin o, first and last staged entry) -- for the
+//          current batch and the next two;
+//   raw    [pulses_per_batch][raw_w] float2 -- the next batch's compressed samples, gathered by
+//          asynchronous copies while the current batch is computed;
+//   stage  [pulses_per_batch][w] float4 -- the current batch's (tau, sigma) entries.
+// Per batch: issue the copies for batch b+1, prefetch the parameters of batch b+2, run the pixel
+// loop of batch b, then (one barrier later) turn the raw samples of b+1 into (tau, sigma) entries.
 template <bool kCheck, bool kPlanar>
 __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
 {
     extern __shared__ float4 smem4[];
+    constexpr int kWarps = kBpThreads / 32;
     const int pb_max = args.pulses_per_batch;
-    float4 *prm = smem4;
-    int4 *win = reinterpret_cast<int4 *>(smem4 + 2 * pb_max);
-    float4 *stage = smem4 + 3 * pb_max;
-    const int w = args.w, wh = args.wh;
+    const int w = args.w, wh = args.wh, rw = args.raw_w;
+    float4 *quads = smem4;                                                   // [3][pb_max][4]
+    int4 *wins = reinterpret_cast<int4 *>(smem4 + 12 * pb_max);              // [3][pb_max]
+    float2 *raw = reinterpret_cast<float2 *>(smem4 + 15 * pb_max);
+    float4 *stage = smem4 + 15 * pb_max + pb_max * rw / 2;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kRowWarps = kBpTileY / kBpRowsPerThread;          // warps per column group (8)
@@ -106,167 +306,125 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
     const int tile_x = blockIdx.x, tile_y = blockIdx.y, slice = blockIdx.z;
     const int p_begin = args.pulse_begin + slice * args.slice_len;
     const int p_end = min(args.pulse_end, p_begin + args.slice_len);
-    // tile centre (float64) and this thread's pixel offsets from it (float32)
-    const double cx = args.x0 + ((double)tile_x * kBpTileX + 0.5 * (kBpTileX - 1)) * args.dx;
-    const double cy = args.y0 + ((double)tile_y * kBpTileY + 0.5 * (kBpTileY - 1)) * args.dy;
-    const float hx = 0.5f * (kBpTileX - 1) * args.dxf, hy = 0.5f * (kBpTileY - 1) * args.dyf;
+    // this thread's pixel offsets from the tile centre (float32), rows paired (2j, 2j + 1)
     const float ox = ((float)col - 0.5f * (kBpTileX - 1)) * args.dxf;
-    float oy[kBpRowsPerThread], od2[kBpRowsPerThread];
+    const float2 ox2 = f2(ox, ox);
+    float2 oyp[kBpRowsPerThread / 2], odp[kBpRowsPerThread / 2];
 #pragma unroll
-    for (int k = 0; k < kBpRowsPerThread; k++) {
-        const int ly = row0 + k;
-        oy[k] = ((float)ly - 0.5f * (kBpTileY - 1)) * args.dyf;
-        od2[k] = fmaf(ox, ox, oy[k] * oy[k]);
+    for (int j = 0; j < kBpRowsPerThread / 2; j++) {
+        const float y0 = ((float)(row0 + 2 * j) - 0.5f * (kBpTileY - 1)) * args.dyf;
+        const float y1 = ((float)(row0 + 2 * j + 1) - 0.5f * (kBpTileY - 1)) * args.dyf;
+        oyp[j] = f2(y0, y1);
+        odp[j] = f2(fmaf(ox, ox, y0 * y0), fmaf(ox, ox, y1 * y1));
     }
-    float acc_re[kBpRowsPerThread], acc_im[kBpRowsPerThread];
+    // complex sums of rows (2j, 2j + 1): real parts and imaginary parts
+    float2 acc_r[kBpRowsPerThread / 2], acc_i[kBpRowsPerThread / 2];
 #pragma unroll
-    for (int k = 0; k < kBpRowsPerThread; k++) acc_re[k] = acc_im[k] = 0.0f;
+    for (int j = 0; j < kBpRowsPerThread / 2; j++) acc_r[j] = acc_i[j] = f2(0.0f, 0.0f);
 
     // entry e of pulse row p lives at stage_row0 + 16 (p w + e); the address of entry round(qm) + wh
     // is formed from the bit pattern of qm + magic with 32-bit wrap-around
     const unsigned stage_row0 = (unsigned)__cvta_generic_to_shared(stage) + 16u * (unsigned)wh - 16u * kRoundMagicBits;
+    const unsigned raw_base = (unsigned)__cvta_generic_to_shared(raw);
     const int ns = args.n_samples;
+    // this tile's rows of the parameter table, indexed by pulse - pulse_begin
+    const int64_t npulses = args.pulse_end - args.pulse_begin;
+    const float4 *tab = args.table + 3 * (((int64_t)tile_y * args.tiles_x + tile_x) * npulses - args.pulse_begin);
 
-    for (int n0 = p_begin; n0 < p_end; n0 += pb_max) {
-        const int pb = min(pb_max, p_end - n0);
-        // ---- per-(tile, pulse) reference range in float64, window extent in float32
-        if (threadIdx.x < pb) {
-            const int n = n0 + threadIdx.x;
-            const double wx = cx - args.pos[3 * n + 0];
-            const double wy = cy - args.pos[3 * n + 1];
-            const double wz = args.z0 - args.pos[3 * n + 2];
-            const double r2 = fma(wx, wx, fma(wy, wy, wz * wz));
-            const float s0 = sqrtf((float)r2);
-            const double s0d = (double)s0;
-            const float res = (float)fma(-s0d, s0d, r2);                  // r2 - s0^2, exact enough in float
-            const double r0 = s0d + (double)(res * (0.5f / s0));          // one Newton step
-            const double qg = (r0 - args.range_start) * args.inv_dr;       // fractional global bin of the centre
-            // Validity: finite, far enough for the range expansion (which bounds every pixel's offset
-            // inside the staged window), and a representable window origin.  Otherwise flag the plan
-            // and zero this pulse's parameters: every pixel then reads entry wh, inside the window.
-            const bool ok = (r0 >= (double)args.min_range_tiles) && (fabs(qg) < 1.0e9);
-            const double o = ok ? floor(qg) : 0.0;
-            // 1 / (r0 dr) to float64 accuracy: float reciprocal refined by one Newton step
-            const float inv_f = 1.0f / (float)r0;
-            const double inv_r0d = (double)inv_f * fma(-r0, (double)inv_f, 2.0);
-            const double kk = inv_r0d * args.inv_dr;
-            const float e = args.dr * (float)inv_r0d;
-            float4 pa, pc;
-            pa.x = (float)(2.0 * wx * kk);          // each coefficient rounded to float once
-            pa.y = (float)(2.0 * wy * kk);
-            pa.z = (float)kk;
-            pa.w = (float)(qg - o) - 0.5f;
-            pc.x = -0.125f * e;
-            pc.y = 0.0625f * e * e;
-            pc.z = -0.0390625f * e * e * e;
-            double t = fma(args.kappa, o + 0.5, args.phase0_turns);
-            t -= rint(t);
-            pc.w = (float)(6.283185307179586 * t);
-            // staged entries: the tile's nearest and farthest pixel ranges (float32 is ample here)
-            // bound every pixel's bin; two entries of margin on each side
-            const float wxf = (float)wx, wyf = (float)wy, wzf = (float)wz;
-            const float nx_ = wxf + fminf(fmaxf(-wxf, -hx), hx), ny_ = wyf + fminf(fmaxf(-wyf, -hy), hy);
-            const float fx = fabsf(wxf) + hx, fy = fabsf(wyf) + hy;
-            const float rmin = sqrtf(fmaf(nx_, nx_, fmaf(ny_, ny_, wzf * wzf)));
-            const float rmax = sqrtf(fmaf(fx, fx, fmaf(fy, fy, wzf * wzf)));
-            const float r0f = (float)r0, qc = (float)(qg - o), idr = (float)args.inv_dr;
-            int e_lo = (int)floorf(fmaf(rmin - r0f, idr, qc)) - 2 + wh;
-            int e_hi = (int)floorf(fmaf(rmax - r0f, idr, qc)) + 2 + wh;
-            e_lo = max(e_lo, 0);
-            e_hi = min(e_hi, w - 1);
-            if (!ok) {
-                pa = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                pc = pa;
-                e_lo = e_hi = wh;
-                atomicOr(args.err, kDevErrGeometry);
-            }
-            prm[2 * threadIdx.x] = pa;
-            prm[2 * threadIdx.x + 1] = pc;
-            win[threadIdx.x] = make_int4((int)o, e_lo, e_hi, 0);
-        }
-        __syncthreads();
-        // ---- stage the windows, one warp per pulse row: entry e <-> global bin o + e - wh holds
-        // (tau, sigma) of samples v_I, v_{I+1}.  Lane j of a row handles the aligned sample pair
-        // (a0 + 2j, a0 + 2j + 1) plus the next sample, which give two consecutive entries.
-        if (kPlanar) {
-            // polyphase planes: sample I at (I & u_mask) Nr + (I >> u_shift).  Each lane loads one sample;
-            // the next one comes from the neighbouring lane (the last lane loads its own).
-            for (int p = warp; p < pb; p += kBpThreads / 32) {
-                const int4 wv = win[p];
-                const float2 *line = args.rc + (int64_t)(n0 + p) * ns;
-                const int first = wv.x - wh + wv.y;
-                const int count = wv.z - wv.y + 1;
-                float4 *row = stage + p * w + wv.y;
-                const float im0 = (float)(wv.y - wh) - 0.5f;
-                for (int c0 = 0; c0 <= count; c0 += 32) {
-                    const int c = c0 + lane;
-                    const int I = first + c;
-                    float2 v0 = make_float2(0.0f, 0.0f), v1;
-                    if (c <= count && I >= 0 && I < ns)
-                        v0 = __ldg(line + (I & args.u_mask) * args.n_range + (I >> args.u_shift));
-                    v1.x = __shfl_down_sync(0xffffffffu, v0.x, 1);
-                    v1.y = __shfl_down_sync(0xffffffffu, v0.y, 1);
-                    if (lane == 31) {
-                        const int J = I + 1;
-                        v1 = (c < count && J >= 0 && J < ns)
-                                 ? __ldg(line + (J & args.u_mask) * args.n_range + (J >> args.u_shift))
-                                 : make_float2(0.0f, 0.0f);
-                    }
-                    if (c < count) {
-                        const float sr = v1.x - v0.x, si = v1.y - v0.y;
-                        const float im = im0 + (float)c;
-                        row[c] = make_float4(fmaf(-im, sr, v0.x), fmaf(-im, si, v0.y), sr, si);
-                    }
-                }
-            }
-        } else
-        for (int p = warp; p < pb; p += kBpThreads / 32) {
+    // asynchronous gather of batch rows [0, count) starting at pulse n into raw: sample j of row p is
+    // the line's sample o - wh + e_lo + j (zero outside the line)
+    auto issue_raw = [&](int n, int count, const int4 *win) {
+        for (int p = warp; p < count; p += kWarps) {
             const int4 wv = win[p];
-            const float2 *line = args.rc + (int64_t)(n0 + p) * ns;
-            const int first = wv.x - wh + wv.y;                 // global bin of entry e_lo
-            const int count = wv.z - wv.y + 1;                  // entries to stage
-            const int a0 = first & ~1;                          // even, so the pair load is 16-byte aligned
-            const int off = first - a0;
-            const int npairs = (count + 1 + off) >> 1;
-            const bool inside = a0 >= 0 && a0 + 2 * npairs < ns;
-            float4 *row = stage + p * w + wv.y;
-            float im = (float)(wv.y - wh) - 0.5f + (float)(2 * lane - off);   // (entry - wh) - 1/2
-            for (int j = lane; j < npairs; j += 32, im += 64.0f) {
-                const int s = a0 + 2 * j;
-                float2 va, vb, vc;
-                if (inside) {
-                    const float4 ab = __ldg(reinterpret_cast<const float4 *>(line + s));
-                    va = make_float2(ab.x, ab.y);
-                    vb = make_float2(ab.z, ab.w);
-                    vc = __ldg(line + s + 2);
-                } else {
-                    const float2 z = make_float2(0.0f, 0.0f);
-                    va = (s >= 0 && s < ns) ? __ldg(line + s) : z;
-                    vb = (s + 1 >= 0 && s + 1 < ns) ? __ldg(line + s + 1) : z;
-                    vc = (s + 2 >= 0 && s + 2 < ns) ? __ldg(line + s + 2) : z;
-                }
-                const int c = 2 * j - off;                      // entry of the pair's first sample
-                if (c >= 0) {
-                    const float sr = vb.x - va.x, si = vb.y - va.y;
-                    row[c] = make_float4(fmaf(-im, sr, va.x), fmaf(-im, si, va.y), sr, si);
-                }
-                if (c + 1 < count) {
-                    const float sr = vc.x - vb.x, si = vc.y - vb.y, im1 = im + 1.0f;
-                    row[c + 1] = make_float4(fmaf(-im1, sr, vb.x), fmaf(-im1, si, vb.y), sr, si);
-                }
+            const int first = wv.x - wh + wv.y;
+            const int nsamp = min(wv.z - wv.y + 2, rw);        // never past the row, whatever the table says
+            const float2 *line = args.rc + (int64_t)(n + p) * ns;
+            const unsigned dst = raw_base + (unsigned)(p * rw) * 8u;
+            for (int j = lane; j < nsamp; j += 32) {
+                const int I = first + j;
+                const bool ok = I >= 0 && I < ns;
+                const int off = kPlanar ? (I & args.u_mask) * args.n_range + (I >> args.u_shift) : I;
+                cp_async8(dst + 8u * (unsigned)j, ok ? (const void *)(line + off) : (const void *)line, ok ? 8 : 0);
             }
         }
-        __syncthreads();
+        cp_async_commit();
+    };
+    // raw samples -> (tau, sigma) entries of the staged windows
+    auto transform = [&](int count, const int4 *win) {
+        for (int p = warp; p < count; p += kWarps) {
+            const int4 wv = win[p];
+            const int e_lo = min(max(wv.y, 0), w - 1);
+            const int nent = min(wv.z - e_lo + 1, min(w - e_lo, rw - 1));   // stays inside both rows
+            const float2 *rr = raw + p * rw;
+            float4 *row = stage + p * w + e_lo;
+            const float im0 = (float)(e_lo - wh) - 0.5f;
+            for (int c = lane; c < nent; c += 32) {
+                const float2 v0 = rr[c], v1 = rr[c + 1];
+                const float sr = v1.x - v0.x, si = v1.y - v0.y;
+                const float im = im0 + (float)c;
+                row[c] = make_float4(fmaf(-im, sr, v0.x), fmaf(-im, si, v0.y), sr, si);
+            }
+        }
+    };
+    // one pulse's table entry -> its slot of the pair quads and its window
+    auto put_params = [&](int p, const float4 pa, const float4 pc, const float4 wf, float4 *quad, int4 *win) {
+        quad[4 * p] = make_float4(pa.x, pa.x, pa.y, pa.y);
+        quad[4 * p + 1] = make_float4(pa.z, pa.z, pa.w, pa.w);
+        quad[4 * p + 2] = make_float4(pc.x, pc.x, pc.y, pc.y);
+        quad[4 * p + 3] = make_float4(pc.z, pc.z, pc.w, pc.w);
+        win[p] = make_int4(__float_as_int(wf.x), __float_as_int(wf.y), __float_as_int(wf.z), 0);
+    };
+    auto load_params = [&](int n, int count, float4 *quad, int4 *win) {
+        if ((int)threadIdx.x < count) {
+            const float4 *src = tab + 3 * (int64_t)(n + threadIdx.x);
+            put_params(threadIdx.x, __ldg(src), __ldg(src + 1), __ldg(src + 2), quad, win);
+        }
+    };
+
+    // prologue: parameters of the first two batches, then the first batch's windows
+    int pb = max(0, min(pb_max, p_end - p_begin));
+    int pb1 = max(0, min(pb_max, p_end - (p_begin + pb)));
+    load_params(p_begin, pb, quads, wins);
+    load_params(p_begin + pb, pb1, quads + 4 * pb_max, wins + pb_max);
+    __syncthreads();
+    if (pb > 0) issue_raw(p_begin, pb, wins);
+    cp_async_wait_all();
+    __syncthreads();
+    if (pb > 0) transform(pb, wins);
+    __syncthreads();
+
+    int buf = 0;
+    for (int n0 = p_begin; n0 < p_end; buf = (buf == 2) ? 0 : buf + 1) {
+        const int buf1 = (buf == 2) ? 0 : buf + 1, buf2 = (buf1 == 2) ? 0 : buf1 + 1;
+        const float4 *quad = quads + 4 * pb_max * buf;
+        const int4 *win = wins + pb_max * buf;
+        const int n1 = n0 + pb, n2 = n1 + pb1;
+        const int pb2 = max(0, min(pb_max, p_end - n2));
+        // the next batch's samples, copied while this batch is computed
+        if (pb1 > 0) issue_raw(n1, pb1, wins + pb_max * buf1);
+        // the batch after next: parameters into registers now, into shared memory after the loop
+        float4 nx0, nx1, nx2;
+        if (warp == 0 && lane < pb2) {
+            const float4 *src = tab + 3 * (int64_t)(n2 + lane);
+            nx0 = __ldg(src);
+            nx1 = __ldg(src + 1);
+            nx2 = __ldg(src + 2);
+        }
         // ---- pixel x pulse inner loop
 #pragma unroll 2
         for (int p = 0; p < pb; p++) {
-            const float4 pa = prm[2 * p], pc = prm[2 * p + 1];
             const int4 wv = kCheck ? win[p] : make_int4(0, 0, 0, 0);
-            const unsigned base = stage_row0 + (unsigned)(p * w) * 16u;
-            const float adx = pa.x * ox;
-            pixel_pulse<kCheck>(pa, pc, wv, base, adx, oy, od2, acc_re, acc_im, args);
+            pixel_pulse<kCheck>(quad + 4 * p, wv, stage_row0 + (unsigned)(p * w) * 16u, ox2, oyp, odp, acc_r, acc_i,
+                                args);
         }
+        if (warp == 0 && lane < pb2) put_params(lane, nx0, nx1, nx2, quads + 4 * pb_max * buf2, wins + pb_max * buf2);
+        cp_async_wait_all();
         __syncthreads();
+        if (pb1 > 0) transform(pb1, wins + pb_max * buf1);
+        __syncthreads();
+        n0 = n1;
+        pb = pb1;
+        pb1 = pb2;
     }
     // ---- store: straight into the image with one slice, else into this slice's partial image
     const int ix = tile_x * kBpTileX + col;
@@ -277,7 +435,7 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
         const int iy = tile_y * kBpTileY + row0 + k;
         if (ix < args.nx && iy < args.ny) {
             float2 *dst = out + (int64_t)iy * args.nx + ix;
-            float2 v = make_float2(acc_re[k], acc_im[k]);
+            float2 v = (k & 1) ? make_float2(acc_r[k / 2].y, acc_i[k / 2].y) : make_float2(acc_r[k / 2].x, acc_i[k / 2].x);
             if (direct && args.accumulate) {
                 const float2 old = *dst;
                 v.x += old.x;
@@ -308,7 +466,8 @@ __global__ void bp_reduce_kernel(const float2 *__restrict__ partial, int slices,
 
 size_t bp_smem_bytes(int w, int pulses_per_batch)
 {
-    return (size_t)pulses_per_batch * (3 + (size_t)w) * sizeof(float4);
+    const size_t raw_w = (size_t)((w + 3) & ~1);
+    return (size_t)pulses_per_batch * ((15 + (size_t)w) * sizeof(float4) + raw_w * sizeof(float2));
 }
 
 cudaError_t bp_configure(int smem_bytes)
@@ -333,6 +492,13 @@ int bp_ctas_per_sm(int smem_bytes)
 cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s)
 {
     if (a.pulse_end <= a.pulse_begin) return cudaSuccess;
+    const int npulse = a.pulse_end - a.pulse_begin;
+    bp_split_pos_kernel<<<(npulse + 255) / 256, 256, 0, s>>>(a.pos, a.pos_split, a.pulse_begin, a.pulse_end);
+    const int64_t entries = (int64_t)npulse * a.tiles_x * a.tiles_y;
+    const int64_t prep_blocks = (entries + 255) / 256;
+    bp_prep_kernel<<<(unsigned)(prep_blocks < (1 << 20) ? prep_blocks : (1 << 20)), 256, 0, s>>>(a);
+    cudaError_t pe = cudaGetLastError();
+    if (pe != cudaSuccess) return pe;
     const dim3 grid(a.tiles_x, a.tiles_y, slices);
     const size_t smem = bp_smem_bytes(a.w, a.pulses_per_batch);
     if (check_bounds) {

@@ -24,6 +24,8 @@ struct sar_plan_s {
     int bp_slots = 1;                 // CTAs of bp_kernel resident on the whole device at once
     int bp_max_slices = 1;            // pulse slices the partial-image buffer can hold
     float2 *d_partial = nullptr;      // [bp_max_slices][ny][nx] partial images
+    float4 *d_table = nullptr;        // [tiles][n_pulses] x 48 B per-(tile, pulse) parameters
+    float2 *d_pos_split = nullptr;    // [n_pulses][3] double-float antenna positions
     // device error word and its pinned host mirror
     int *d_err = nullptr;
     int *h_err = nullptr;
@@ -204,6 +206,12 @@ int bp_pick_slices(sar_plan p, int pulses)
     return best;
 }
 
+float2 split_double(double v)
+{
+    const float hi = (float)v;
+    return make_float2(hi, (float)(v - (double)hi));
+}
+
 sar_status setup_bp(sar_plan p)
 {
     const sar_radar &r = p->radar;
@@ -234,6 +242,15 @@ sar_status setup_bp(sar_plan p)
     const double ph = 2.0 * r.range_start / lambda;
     a.phase0_turns = ph - std::floor(ph);
     a.kappa = 2.0 * dr / lambda;
+    a.x0s = split_double(g.x0);
+    a.y0s = split_double(g.y0);
+    a.z0s = split_double(g.z0);
+    a.dxs = split_double(g.dx);
+    a.dys = split_double(g.dy);
+    a.rss = split_double(r.range_start);
+    a.idrs = split_double(1.0 / dr);
+    a.ph0s = split_double(a.phase0_turns);
+    a.kps = split_double(a.kappa);
     a.two_pi_kappa = (float)(2.0 * M_PI * a.kappa);
     // window: every pixel of a tile lies within the half-diagonal r_t of its centre, so its range lies
     // within r_t of the centre's range; wh bins on each side plus margin for the float32 offsets
@@ -242,15 +259,25 @@ sar_status setup_bp(sar_plan p)
     a.wh = (int)std::ceil(rt / dr) + 3;
     a.w = 2 * a.wh + 1;
     a.min_range_tiles = (float)(100.0 * rt);
-    // pulses per batch: as many as fit 108 KB of staging (two CTAs per SM), between 4 and 32
-    int pb = (int)((108 * 1024) / (((size_t)a.w + 3) * sizeof(float4)));
+    // pulses per batch: as many as fit 100 KB of staging (two CTAs per SM), between 4 and 32
+    a.raw_w = (a.w + 3) & ~1;
+    int pb = (int)((100 * 1024) / sar::bp_smem_bytes(a.w, 1));
     if (pb > 32) pb = 32;
+    pb &= ~1;                     // even: the kernel keeps pulse parameters in (pulse, pulse + 1) pairs
     if (pb < 4) {
         pb = 4;
         if (sar::bp_smem_bytes(a.w, pb) > 200 * 1024) return SAR_ERR_UNSUPPORTED;   // pixels too coarse for a tile
     }
     a.pulses_per_batch = pb;
     a.err = p->d_err;
+    {
+        const size_t entries = (size_t)a.tiles_x * a.tiles_y * r.n_pulses;
+        cudaError_t et = cudaMalloc(&p->d_table, entries * 3 * sizeof(float4));
+        if (et == cudaSuccess) et = cudaMalloc(&p->d_pos_split, (size_t)r.n_pulses * 3 * sizeof(float2));
+        if (et != cudaSuccess) return cuda_status(et);
+        a.table = p->d_table;
+        a.pos_split = p->d_pos_split;
+    }
     const int smem = (int)sar::bp_smem_bytes(a.w, pb);
     cudaError_t e = sar::bp_configure(smem);
     if (e != cudaSuccess) return cuda_status(e);
@@ -275,6 +302,8 @@ void free_plan(sar_plan p)
     if (!p) return;
     cudaFree(p->d_tables);
     cudaFree(p->d_partial);
+    cudaFree(p->d_table);
+    cudaFree(p->d_pos_split);
     cudaFree(p->d_err);
     if (p->h_err) cudaFreeHost(p->h_err);
     cudaFree(p->d_raw);
@@ -304,7 +333,7 @@ sar_status do_backproject(sar_plan plan, const void *rc, const double *pos, int3
     a.slice_len = (pulse_count + slices - 1) / slices;
     a.partial = plan->d_partial;
     a.planar = (layout == SAR_RC_POLYPHASE && plan->radar.upsample > 1) ? 1 : 0;
-    plan->last_launches += slices > 1 ? 2 : 1;
+    plan->last_launches += slices > 1 ? 4 : 3;
     return cuda_status(sar::launch_bp(a, slices, plan->check_bounds, s));
 }
 

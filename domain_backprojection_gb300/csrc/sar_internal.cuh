@@ -64,12 +64,18 @@ struct BpArgs {
     float two_pi_kappa;      // 2 pi kappa (rad per bin)
     // staged window: entries e in [0, w) hold local bins i = e - wh
     int wh, w;
+    int raw_w;               // raw samples per staged row: w + 1, rounded up to even
     int pulses_per_batch;
     float min_range_tiles;   // geometry validity: range >= this (m) per tile
     // pulse slicing: slice s of gridDim.z sums pulses [pulse_begin + s * slice_len, ...) into
     // partial + s * nx * ny (or straight into image when there is one slice)
     int slice_len;
     float2 *partial;
+    // per (tile, pulse) parameters written by the prep kernel: 3 float4 per entry
+    float4 *table;
+    // double-float (hi, lo) copies of the float64 constants the prep kernel needs, and of the positions
+    float2 x0s, y0s, z0s, dxs, dys, rss, idrs, ph0s, kps;
+    float2 *pos_split;       // [Na][3]
     // data
     const float2 *rc;        // [Na][U Nr], natural order or polyphase planes (planar != 0)
     int planar, u_shift, u_mask, n_range;   // planes: sample I of a line at (I & u_mask) Nr + (I >> u_shift)

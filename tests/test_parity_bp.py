@@ -34,7 +34,7 @@ def test_form_image_full(scenes, cfg):
     plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
     img = sar.sar_form_image(plan, s["raw"], s["pos"])
     sar.sar_plan_sync(plan)
-    assert sar.sar_plan_last_launches(plan) in (2, 3)   # range compression, backprojection (+ slice reduction)
+    assert 2 <= sar.sar_plan_last_launches(plan) <= 5   # range compression, position split, tile prep, pixel loop (+ slice sum)
     rc = _oracle_rc(s)
     ref = oracle.backproject(s["radar"], s["grid"], rc, s["pos"].cpu().numpy(), threads=ORACLE_THREADS)
     got = img.cpu().numpy()
