@@ -282,7 +282,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 //   params [3][pulses_per_batch][4] float4 parameter quads (see pixel_pulse) and
 //          [3][pulses_per_batch] int4 windows (origin o, first and last staged entry) -- for the
 //          current batch and the next two;
-//   raw    [pulses_per_batch][raw_w] float2 -- the next batch's compressed samples, gathered by
+//   raw    [batch][rw] float2 -- the next batch's compressed samples, gathered by
 //          asynchronous copies while the current batch is computed;
 //   stage  [pulses_per_batch][w] float4 -- the current batch's (tau, sigma) entries.
 // Per batch: issue the copies for batch b+1, prefetch the parameters of batch b+2, run the pixel
@@ -292,13 +292,11 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
 {
     extern __shared__ float4 smem4[];
     constexpr int kWarps = kBpThreads / 32;
-    const int pb_max = args.pulses_per_batch;
-    const int w = args.w, wh = args.wh, rw = args.raw_w;
-    float4 *quads = smem4;                                                   // [3][pb_max][4]
-    int4 *wins = reinterpret_cast<int4 *>(smem4 + 12 * pb_max);              // [3][pb_max]
-    float2 *raw = reinterpret_cast<float2 *>(smem4 + 15 * pb_max);
-    float4 *stage = smem4 + 15 * pb_max + pb_max * rw / 2;
-
+    const int pb_cap = args.pulses_per_batch;                                 // parameter slots per batch
+    const int wh = args.wh;
+    float4 *quads = smem4;                                                   // [3][pb_cap][4]
+    int4 *wins = reinterpret_cast<int4 *>(smem4 + 12 * pb_cap);              // [3][pb_cap]
+    float4 *dyn = smem4 + 15 * pb_cap;                                       // raw rows, then stage rows
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kRowWarps = kBpTileY / kBpRowsPerThread;          // warps per column group (8)
     const int col = (warp / kRowWarps) * 32 + lane;                  // pixel column inside the tile
@@ -322,14 +320,39 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
 #pragma unroll
     for (int j = 0; j < kBpRowsPerThread / 2; j++) acc_r[j] = acc_i[j] = f2(0.0f, 0.0f);
 
-    // entry e of pulse row p lives at stage_row0 + 16 (p w + e); the address of entry round(qm) + wh
-    // is formed from the bit pattern of qm + magic with 32-bit wrap-around
-    const unsigned stage_row0 = (unsigned)__cvta_generic_to_shared(stage) + 16u * (unsigned)wh - 16u * kRoundMagicBits;
-    const unsigned raw_base = (unsigned)__cvta_generic_to_shared(raw);
     const int ns = args.n_samples;
     // this tile's rows of the parameter table, indexed by pulse - pulse_begin
     const int64_t npulses = args.pulse_end - args.pulse_begin;
     const float4 *tab = args.table + 3 * (((int64_t)tile_y * args.tiles_x + tile_x) * npulses - args.pulse_begin);
+
+    // Row sizes from the windows this CTA will actually stage (at most the diagonal bound w): the
+    // widest window of the slice sets the stage row stride, and as many pulses as fit the shared
+    // memory make a batch.
+    __shared__ int s_extent;
+    if (threadIdx.x == 0) s_extent = 1;
+    __syncthreads();
+    {
+        int m = 1;
+        for (int n = p_begin + (int)threadIdx.x; n < p_end; n += kBpThreads) {
+            const float4 wf = __ldg(tab + 3 * (int64_t)n + 2);
+            m = max(m, __float_as_int(wf.z) - __float_as_int(wf.y) + 1);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) atomicMax(&s_extent, m);
+    }
+    __syncthreads();
+    const int stride = min(s_extent, args.w);                                // stage entries per row
+    const int rw = (stride + 3) & ~1;                                        // raw samples per row (> stride)
+    const int pb_max = max(1, min(pb_cap, args.stage_bytes / (stride * 16 + rw * 8)));
+    float2 *raw = reinterpret_cast<float2 *>(dyn);                           // [pb_max][rw]
+    float4 *stage = dyn + pb_max * rw / 2;                                   // [pb_max][stride]
+
+    // entry e of pulse row p lives at stage + p stride + e - e_lo(p); win.w holds p stride - e_lo(p),
+    // and the address of entry round(qm) + wh is formed from the bit pattern of qm + magic with
+    // 32-bit wrap-around
+    const unsigned stage_row0 = (unsigned)__cvta_generic_to_shared(stage) + 16u * (unsigned)wh - 16u * kRoundMagicBits;
+    const unsigned raw_base = (unsigned)__cvta_generic_to_shared(raw);
 
     // asynchronous gather of batch rows [0, count) starting at pulse n into raw: sample j of row p is
     // the line's sample o - wh + e_lo + j (zero outside the line)
@@ -337,7 +360,7 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
         for (int p = warp; p < count; p += kWarps) {
             const int4 wv = win[p];
             const int first = wv.x - wh + wv.y;
-            const int nsamp = min(wv.z - wv.y + 2, rw);        // never past the row, whatever the table says
+            const int nsamp = min(wv.z - wv.y + 2, rw);        // never past the row
             const float2 *line = args.rc + (int64_t)(n + p) * ns;
             const unsigned dst = raw_base + (unsigned)(p * rw) * 8u;
             for (int j = lane; j < nsamp; j += 32) {
@@ -353,10 +376,10 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
     auto transform = [&](int count, const int4 *win) {
         for (int p = warp; p < count; p += kWarps) {
             const int4 wv = win[p];
-            const int e_lo = min(max(wv.y, 0), w - 1);
-            const int nent = min(wv.z - e_lo + 1, min(w - e_lo, rw - 1));   // stays inside both rows
+            const int e_lo = wv.y;
+            const int nent = min(wv.z - e_lo + 1, stride);                  // stays inside both rows
             const float2 *rr = raw + p * rw;
-            float4 *row = stage + p * w + e_lo;
+            float4 *row = stage + p * stride;
             const float im0 = (float)(e_lo - wh) - 0.5f;
             for (int c = lane; c < nent; c += 32) {
                 const float2 v0 = rr[c], v1 = rr[c + 1];
@@ -372,7 +395,8 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
         quad[4 * p + 1] = make_float4(pa.z, pa.z, pa.w, pa.w);
         quad[4 * p + 2] = make_float4(pc.x, pc.x, pc.y, pc.y);
         quad[4 * p + 3] = make_float4(pc.z, pc.z, pc.w, pc.w);
-        win[p] = make_int4(__float_as_int(wf.x), __float_as_int(wf.y), __float_as_int(wf.z), 0);
+        const int e_lo = __float_as_int(wf.y);
+        win[p] = make_int4(__float_as_int(wf.x), e_lo, __float_as_int(wf.z), p * stride - e_lo);
     };
     auto load_params = [&](int n, int count, float4 *quad, int4 *win) {
         if ((int)threadIdx.x < count) {
@@ -385,7 +409,7 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
     int pb = max(0, min(pb_max, p_end - p_begin));
     int pb1 = max(0, min(pb_max, p_end - (p_begin + pb)));
     load_params(p_begin, pb, quads, wins);
-    load_params(p_begin + pb, pb1, quads + 4 * pb_max, wins + pb_max);
+    load_params(p_begin + pb, pb1, quads + 4 * pb_cap, wins + pb_cap);
     __syncthreads();
     if (pb > 0) issue_raw(p_begin, pb, wins);
     cp_async_wait_all();
@@ -396,16 +420,16 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
     int buf = 0;
     for (int n0 = p_begin; n0 < p_end; buf = (buf == 2) ? 0 : buf + 1) {
         const int buf1 = (buf == 2) ? 0 : buf + 1, buf2 = (buf1 == 2) ? 0 : buf1 + 1;
-        const float4 *quad = quads + 4 * pb_max * buf;
-        const int4 *win = wins + pb_max * buf;
+        const float4 *quad = quads + 4 * pb_cap * buf;
+        const int4 *win = wins + pb_cap * buf;
         const int n1 = n0 + pb, n2 = n1 + pb1;
         const int pb2 = max(0, min(pb_max, p_end - n2));
         // the next batch's samples, copied while this batch is computed
-        if (pb1 > 0) issue_raw(n1, pb1, wins + pb_max * buf1);
+        if (pb1 > 0) issue_raw(n1, pb1, wins + pb_cap * buf1);
         // the batch after next: parameters into registers now, into shared memory after the loop
         float4 nx0, nx1, nx2;
-        if (warp == 0 && lane < pb2) {
-            const float4 *src = tab + 3 * (int64_t)(n2 + lane);
+        if ((int)threadIdx.x < pb2) {
+            const float4 *src = tab + 3 * (int64_t)(n2 + threadIdx.x);
             nx0 = __ldg(src);
             nx1 = __ldg(src + 1);
             nx2 = __ldg(src + 2);
@@ -413,14 +437,13 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
         // ---- pixel x pulse inner loop
 #pragma unroll 2
         for (int p = 0; p < pb; p++) {
-            const int4 wv = kCheck ? win[p] : make_int4(0, 0, 0, 0);
-            pixel_pulse<kCheck>(quad + 4 * p, wv, stage_row0 + (unsigned)(p * w) * 16u, ox2, oyp, odp, acc_r, acc_i,
-                                args);
+            const int4 wv = win[p];
+            pixel_pulse<kCheck>(quad + 4 * p, wv, stage_row0 + (unsigned)wv.w * 16u, ox2, oyp, odp, acc_r, acc_i, args);
         }
-        if (warp == 0 && lane < pb2) put_params(lane, nx0, nx1, nx2, quads + 4 * pb_max * buf2, wins + pb_max * buf2);
+        if ((int)threadIdx.x < pb2) put_params(threadIdx.x, nx0, nx1, nx2, quads + 4 * pb_cap * buf2, wins + pb_cap * buf2);
         cp_async_wait_all();
         __syncthreads();
-        if (pb1 > 0) transform(pb1, wins + pb_max * buf1);
+        if (pb1 > 0) transform(pb1, wins + pb_cap * buf1);
         __syncthreads();
         n0 = n1;
         pb = pb1;
@@ -464,10 +487,9 @@ __global__ void bp_reduce_kernel(const float2 *__restrict__ partial, int slices,
 
 }  // namespace
 
-size_t bp_smem_bytes(int w, int pulses_per_batch)
+size_t bp_smem_bytes(const BpArgs &a)
 {
-    const size_t raw_w = (size_t)((w + 3) & ~1);
-    return (size_t)pulses_per_batch * ((15 + (size_t)w) * sizeof(float4) + raw_w * sizeof(float2));
+    return (size_t)15 * a.pulses_per_batch * sizeof(float4) + (size_t)a.stage_bytes;
 }
 
 cudaError_t bp_configure(int smem_bytes)
@@ -500,7 +522,7 @@ cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream
     cudaError_t pe = cudaGetLastError();
     if (pe != cudaSuccess) return pe;
     const dim3 grid(a.tiles_x, a.tiles_y, slices);
-    const size_t smem = bp_smem_bytes(a.w, a.pulses_per_batch);
+    const size_t smem = bp_smem_bytes(a);
     if (check_bounds) {
         if (a.planar) bp_kernel<true, true><<<grid, kBpThreads, smem, s>>>(a);
         else bp_kernel<true, false><<<grid, kBpThreads, smem, s>>>(a);

@@ -259,16 +259,11 @@ sar_status setup_bp(sar_plan p)
     a.wh = (int)std::ceil(rt / dr) + 3;
     a.w = 2 * a.wh + 1;
     a.min_range_tiles = (float)(100.0 * rt);
-    // pulses per batch: as many as fit 100 KB of staging (two CTAs per SM), between 4 and 32
-    a.raw_w = (a.w + 3) & ~1;
-    int pb = (int)((100 * 1024) / sar::bp_smem_bytes(a.w, 1));
-    if (pb > 32) pb = 32;
-    pb &= ~1;                     // even: the kernel keeps pulse parameters in (pulse, pulse + 1) pairs
-    if (pb < 4) {
-        pb = 4;
-        if (sar::bp_smem_bytes(a.w, pb) > 200 * 1024) return SAR_ERR_UNSUPPORTED;   // pixels too coarse for a tile
-    }
-    a.pulses_per_batch = pb;
+    // 108 KB of shared memory per CTA (two per SM): 48 pulses' parameters, the rest for raw and staged
+    // rows; the kernel sizes its rows from the windows it actually stages
+    a.pulses_per_batch = 48;
+    a.stage_bytes = 108 * 1024 - 15 * a.pulses_per_batch * (int)sizeof(float4);
+    if (a.w * 16 + ((a.w + 3) & ~1) * 8 > a.stage_bytes) return SAR_ERR_UNSUPPORTED;   // pixels too coarse
     a.err = p->d_err;
     {
         const size_t entries = (size_t)a.tiles_x * a.tiles_y * r.n_pulses;
@@ -278,7 +273,7 @@ sar_status setup_bp(sar_plan p)
         a.table = p->d_table;
         a.pos_split = p->d_pos_split;
     }
-    const int smem = (int)sar::bp_smem_bytes(a.w, pb);
+    const int smem = (int)sar::bp_smem_bytes(a);
     cudaError_t e = sar::bp_configure(smem);
     if (e != cudaSuccess) return cuda_status(e);
     int sms = 0;

@@ -63,9 +63,9 @@ struct BpArgs {
     double kappa;            // 2 dr_U / lambda, turns per bin
     float two_pi_kappa;      // 2 pi kappa (rad per bin)
     // staged window: entries e in [0, w) hold local bins i = e - wh
-    int wh, w;
-    int raw_w;               // raw samples per staged row: w + 1, rounded up to even
-    int pulses_per_batch;
+    int wh, w;               // every pixel of a tile reads entries within [0, w) of its pulse's window
+    int pulses_per_batch;    // parameter slots per batch (the batch may be smaller)
+    int stage_bytes;         // shared memory for raw and staged rows of one batch
     float min_range_tiles;   // geometry validity: range >= this (m) per tile
     // pulse slicing: slice s of gridDim.z sums pulses [pulse_begin + s * slice_len, ...) into
     // partial + s * nx * ny (or straight into image when there is one slice)
@@ -86,7 +86,7 @@ struct BpArgs {
     int *err;                // device error word
 };
 
-size_t bp_smem_bytes(int w, int pulses_per_batch);
+size_t bp_smem_bytes(const BpArgs &a);
 cudaError_t bp_configure(int smem_bytes);
 int bp_ctas_per_sm(int smem_bytes);
 cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s);
