@@ -202,10 +202,10 @@ __device__ __forceinline__ void tile_pulse_params(const BpArgs &args, int tile_x
     const dflt ax = {ap[0].x, ap[0].y}, ay = {ap[1].x, ap[1].y}, az = {ap[2].x, ap[2].y};
     // tile centre: x0 + (tile * 64 + 31.5) dx, y0 + (tile * 32 + 15.5) dy (the float multipliers are exact)
     const dflt cx = df_add({args.x0s.x, args.x0s.y},
-                           df_mulf({args.dxs.x, args.dxs.y}, (float)tile_x * kBpTileX + 0.5f * (kBpTileX - 1)));
+                           df_mulf({args.dxs.x, args.dxs.y}, (float)tile_x * args.tile_w + 0.5f * (args.tile_w - 1)));
     const dflt cy = df_add({args.y0s.x, args.y0s.y},
-                           df_mulf({args.dys.x, args.dys.y}, (float)tile_y * kBpTileY + 0.5f * (kBpTileY - 1)));
-    const float hx = 0.5f * (kBpTileX - 1) * args.dxf, hy = 0.5f * (kBpTileY - 1) * args.dyf;
+                           df_mulf({args.dys.x, args.dys.y}, (float)tile_y * args.tile_h + 0.5f * (args.tile_h - 1)));
+    const float hx = 0.5f * (args.tile_w - 1) * args.dxf, hy = 0.5f * (args.tile_h - 1) * args.dyf;
     const dflt wx = df_add(cx, df_neg(ax)), wy = df_add(cy, df_neg(ay)), wz = df_add({args.z0s.x, args.z0s.y}, df_neg(az));
     const dflt r2 = df_add(df_mul(wx, wx), df_add(df_mul(wy, wy), df_mul(wz, wz)));
     const dflt r0 = df_sqrt(r2);
@@ -287,9 +287,10 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 //   stage  [pulses_per_batch][w] float4 -- the current batch's (tau, sigma) entries.
 // Per batch: issue the copies for batch b+1, prefetch the parameters of batch b+2, run the pixel
 // loop of batch b, then (one barrier later) turn the raw samples of b+1 into (tau, sigma) entries.
-template <bool kCheck, bool kPlanar>
+template <int kTileX, bool kCheck, bool kPlanar>
 __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
 {
+    constexpr int kTileY = kBpThreads * kBpRowsPerThread / kTileX;
     extern __shared__ float4 smem4[];
     constexpr int kWarps = kBpThreads / 32;
     const int pb_cap = args.pulses_per_batch;                                 // parameter slots per batch
@@ -298,20 +299,20 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
     int4 *wins = reinterpret_cast<int4 *>(smem4 + 12 * pb_cap);              // [3][pb_cap]
     float4 *dyn = smem4 + 15 * pb_cap;                                       // raw rows, then stage rows
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int kRowWarps = kBpTileY / kBpRowsPerThread;          // warps per column group (8)
+    constexpr int kRowWarps = kTileY / kBpRowsPerThread;            // warps per column group
     const int col = (warp / kRowWarps) * 32 + lane;                  // pixel column inside the tile
     const int row0 = (warp % kRowWarps) * kBpRowsPerThread;          // first of this thread's rows
     const int tile_x = blockIdx.x, tile_y = blockIdx.y, slice = blockIdx.z;
     const int p_begin = args.pulse_begin + slice * args.slice_len;
     const int p_end = min(args.pulse_end, p_begin + args.slice_len);
     // this thread's pixel offsets from the tile centre (float32), rows paired (2j, 2j + 1)
-    const float ox = ((float)col - 0.5f * (kBpTileX - 1)) * args.dxf;
+    const float ox = ((float)col - 0.5f * (kTileX - 1)) * args.dxf;
     const float2 ox2 = f2(ox, ox);
     float2 oyp[kBpRowsPerThread / 2], odp[kBpRowsPerThread / 2];
 #pragma unroll
     for (int j = 0; j < kBpRowsPerThread / 2; j++) {
-        const float y0 = ((float)(row0 + 2 * j) - 0.5f * (kBpTileY - 1)) * args.dyf;
-        const float y1 = ((float)(row0 + 2 * j + 1) - 0.5f * (kBpTileY - 1)) * args.dyf;
+        const float y0 = ((float)(row0 + 2 * j) - 0.5f * (kTileY - 1)) * args.dyf;
+        const float y1 = ((float)(row0 + 2 * j + 1) - 0.5f * (kTileY - 1)) * args.dyf;
         oyp[j] = f2(y0, y1);
         odp[j] = f2(fmaf(ox, ox, y0 * y0), fmaf(ox, ox, y1 * y1));
     }
@@ -450,12 +451,12 @@ __global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
         pb1 = pb2;
     }
     // ---- store: straight into the image with one slice, else into this slice's partial image
-    const int ix = tile_x * kBpTileX + col;
+    const int ix = tile_x * kTileX + col;
     const bool direct = gridDim.z == 1;
     float2 *out = direct ? args.image : args.partial + (int64_t)slice * args.nx * args.ny;
 #pragma unroll
     for (int k = 0; k < kBpRowsPerThread; k++) {
-        const int iy = tile_y * kBpTileY + row0 + k;
+        const int iy = tile_y * kTileY + row0 + k;
         if (ix < args.nx && iy < args.ny) {
             float2 *dst = out + (int64_t)iy * args.nx + ix;
             float2 v = (k & 1) ? make_float2(acc_r[k / 2].y, acc_i[k / 2].y) : make_float2(acc_r[k / 2].x, acc_i[k / 2].x);
@@ -492,10 +493,11 @@ size_t bp_smem_bytes(const BpArgs &a)
     return (size_t)15 * a.pulses_per_batch * sizeof(float4) + (size_t)a.stage_bytes;
 }
 
-cudaError_t bp_configure(int smem_bytes)
+template <int TX>
+cudaError_t bp_configure_shape(int smem_bytes)
 {
-    const void *fns[] = {(const void *)bp_kernel<false, false>, (const void *)bp_kernel<false, true>,
-                         (const void *)bp_kernel<true, false>, (const void *)bp_kernel<true, true>};
+    const void *fns[] = {(const void *)bp_kernel<TX, false, false>, (const void *)bp_kernel<TX, false, true>,
+                         (const void *)bp_kernel<TX, true, false>, (const void *)bp_kernel<TX, true, true>};
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e != cudaSuccess) return e;
@@ -503,10 +505,31 @@ cudaError_t bp_configure(int smem_bytes)
     return cudaSuccess;
 }
 
+cudaError_t bp_configure(int smem_bytes)
+{
+    cudaError_t e = bp_configure_shape<128>(smem_bytes);
+    if (e == cudaSuccess) e = bp_configure_shape<64>(smem_bytes);
+    if (e == cudaSuccess) e = bp_configure_shape<32>(smem_bytes);
+    return e;
+}
+
+template <int TX>
+void launch_bp_shape(const BpArgs &a, dim3 grid, size_t smem, bool check_bounds, cudaStream_t s)
+{
+    if (check_bounds) {
+        if (a.planar) bp_kernel<TX, true, true><<<grid, kBpThreads, smem, s>>>(a);
+        else bp_kernel<TX, true, false><<<grid, kBpThreads, smem, s>>>(a);
+    } else {
+        if (a.planar) bp_kernel<TX, false, true><<<grid, kBpThreads, smem, s>>>(a);
+        else bp_kernel<TX, false, false><<<grid, kBpThreads, smem, s>>>(a);
+    }
+}
+
 int bp_ctas_per_sm(int smem_bytes)
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bp_kernel<false, true>, kBpThreads, smem_bytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bp_kernel<128, false, true>, kBpThreads, smem_bytes) !=
+        cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
 }
@@ -523,13 +546,9 @@ cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream
     if (pe != cudaSuccess) return pe;
     const dim3 grid(a.tiles_x, a.tiles_y, slices);
     const size_t smem = bp_smem_bytes(a);
-    if (check_bounds) {
-        if (a.planar) bp_kernel<true, true><<<grid, kBpThreads, smem, s>>>(a);
-        else bp_kernel<true, false><<<grid, kBpThreads, smem, s>>>(a);
-    } else {
-        if (a.planar) bp_kernel<false, true><<<grid, kBpThreads, smem, s>>>(a);
-        else bp_kernel<false, false><<<grid, kBpThreads, smem, s>>>(a);
-    }
+    if (a.tile_w == 128) launch_bp_shape<128>(a, grid, smem, check_bounds, s);
+    else if (a.tile_w == 64) launch_bp_shape<64>(a, grid, smem, check_bounds, s);
+    else launch_bp_shape<32>(a, grid, smem, check_bounds, s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || slices == 1) return e;
     const int64_t npix = (int64_t)a.nx * a.ny;

@@ -226,8 +226,19 @@ sar_status setup_bp(sar_plan p)
     a.dyf = (float)g.dy;
     a.nx = g.nx;
     a.ny = g.ny;
-    a.tiles_x = (g.nx + sar::kBpTileX - 1) / sar::kBpTileX;
-    a.tiles_y = (g.ny + sar::kBpTileY - 1) / sar::kBpTileY;
+    // tile shape: the longest in azimuth (x) whose half-diagonal stays within 20 m, so that the range
+    // expansion about the tile centre holds from 2 km (100 half-diagonals) outward
+    a.tile_w = 32;
+    for (int tw : {128, 64}) {
+        const int th = sar::kBpThreads * sar::kBpRowsPerThread / tw;
+        if (0.5 * std::hypot((tw - 1) * g.dx, (th - 1) * g.dy) <= 20.0) {
+            a.tile_w = tw;
+            break;
+        }
+    }
+    a.tile_h = sar::kBpThreads * sar::kBpRowsPerThread / a.tile_w;
+    a.tiles_x = (g.nx + a.tile_w - 1) / a.tile_w;
+    a.tiles_y = (g.ny + a.tile_h - 1) / a.tile_h;
     if (a.tiles_y > 65535) return SAR_ERR_UNSUPPORTED;
     const double dr = kC0 / (2.0 * r.fs * r.upsample);
     a.range_start = r.range_start;
@@ -254,7 +265,7 @@ sar_status setup_bp(sar_plan p)
     a.two_pi_kappa = (float)(2.0 * M_PI * a.kappa);
     // window: every pixel of a tile lies within the half-diagonal r_t of its centre, so its range lies
     // within r_t of the centre's range; wh bins on each side plus margin for the float32 offsets
-    const double ex = (sar::kBpTileX - 1) * g.dx, ey = (sar::kBpTileY - 1) * g.dy;
+    const double ex = (a.tile_w - 1) * g.dx, ey = (a.tile_h - 1) * g.dy;
     const double rt = 0.5 * std::sqrt(ex * ex + ey * ey);
     a.wh = (int)std::ceil(rt / dr) + 3;
     a.w = 2 * a.wh + 1;

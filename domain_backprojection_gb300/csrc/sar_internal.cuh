@@ -41,10 +41,9 @@ cudaError_t rc_configure(int n);
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s);
 
 // ----------------------------------------------------------- backprojection
-constexpr int kBpTileX = 64;     // pixels per tile along x (azimuth): two warps' lanes
-constexpr int kBpTileY = 32;     // pixels per tile along y (ground range)
-constexpr int kBpRowsPerThread = 4;
-constexpr int kBpThreads = kBpTileX * kBpTileY / kBpRowsPerThread;   // 512
+constexpr int kBpRowsPerThread = 4;   // pixel rows each thread accumulates
+constexpr int kBpThreads = 512;        // threads per CTA: a tile of kBpThreads * kBpRowsPerThread pixels,
+                                       // 128 x 16, 64 x 32 or 32 x 64 (x along azimuth), chosen per plan
 constexpr int kBpMaxSlices = 32;
 
 struct BpArgs {
@@ -53,6 +52,7 @@ struct BpArgs {
     double dx, dy;           // pixel spacing (float64: tile centres must not inherit float32 rounding)
     float dxf, dyf;          // the same spacing in float32, for offsets inside a tile
     int nx, ny, tiles_x, tiles_y;
+    int tile_w, tile_h;      // tile shape in pixels (tile_w * tile_h = kBpThreads * kBpRowsPerThread)
     // range axis
     double range_start;      // m
     double inv_dr;           // 1 / dr_U (bins per metre)
