@@ -103,17 +103,31 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def kernel_traffic(kernel, src_file):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+KERNEL_SOURCES = {
+    "bp_kernel": ["bp_kernel.cu", "sar_internal.cuh"],
+    "rc_reg_kernel": ["rc_kernel.cu", "sar_internal.cuh"],
+    "rc_fused_kernel": ["rc_kernel.cu", "sar_internal.cuh"],
+}
+
+
+def source_digest(kernel):
+    """sha256 over the source files a kernel is compiled from (concatenated in a fixed order)."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "domain_backprojection_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def kernel_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's sources are unchanged since."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        with open(src_file, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-        if rec.get("source_sha256") == digest:
+        if rec.get("source_sha256") == source_digest(kernel):
             return rec.get("dram_bytes_per_launch")
-    except (OSError, ValueError):
+    except (OSError, ValueError, KeyError):
         pass
     return None
 
@@ -138,20 +152,16 @@ def run_ours(args, rank, world, local_rank):
     img = torch.empty(grid.ny, grid.nx, dtype=torch.complex64, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i, ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def step(i):
         sar.sar_range_compress(plan, raws[i % n_sets], rc, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
         sar.sar_backproject(plan, rc, poss[i % n_sets], 0, cfg.n_pulses, img, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
 
     for i in range(args.warmup):
         step(i)
     sar.sar_plan_sync(plan, stream)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # the library records CUDA events on `stream` around the two main kernels of every timed step
+    sar.sar_plan_set_timing(plan, True)
+    sar.sar_plan_kernel_times(plan)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -160,7 +170,7 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clocks:
         t0.record(stream)
         for i in range(args.steps):
-            step(i, evs[i])
+            step(i)
             launches += 1 + sar.sar_plan_last_launches(plan)
         t1.record(stream)
         torch.cuda.synchronize(dev)
@@ -168,8 +178,11 @@ def run_ours(args, rank, world, local_rank):
             torch.distributed.barrier()
     sar.sar_plan_sync(plan, stream)
     ms_total = t0.elapsed_time(t1)
-    rc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    kt = sar.sar_plan_kernel_times(plan)
+    sar.sar_plan_set_timing(plan, False)
+    assert kt["rc_calls"] == args.steps and kt["bp_calls"] == args.steps, kt
+    rc_ms = kt["rc_ms"] / kt["rc_calls"]
+    bp_ms = kt["bp_ms"] / kt["bp_calls"]
     if world > 1:
         t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -207,7 +220,7 @@ def run_ours(args, rank, world, local_rank):
     n_range, U = radar.n_range, radar.upsample
     rc_bytes = cfg.n_pulses * 8 * n_range * (1 + U)
     rc_gbs = rc_bytes / (rc_ms * 1e-3) / 1e9
-    src = os.path.join(ROOT, "domain_backprojection_gb300", "csrc")
+    rc_name = rc_kernel_name(n_range)
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -220,18 +233,18 @@ def run_ours(args, rank, world, local_rank):
                            "(the kernels sar_form_image runs)"},
         "rc_lines_per_s": round(world * cfg.n_pulses / (rc_ms * 1e-3), 1),
         "bp_gpix_pulse_per_s": round(world * pp / (bp_ms * 1e-3) / 1e9, 3),
-        "kernel_ms": {"rc_fused_kernel": round(rc_ms, 4), "bp_kernel": round(bp_ms, 4)},
+        "kernel_ms": {rc_name: round(rc_ms, 4), "bp_kernel": round(bp_ms, 4)},
         "roofline": {"kernel": "bp_kernel", "bound": "alu", "achieved": round(bp_tflops, 3),
                      "peak": round(fp32_peak, 3), "unit": "TFLOP/s", "frac": round(bp_tflops / fp32_peak, 4),
-                     "traffic": kernel_traffic("bp_kernel", os.path.join(src, "bp_kernel.cu")),
+                     "traffic": kernel_traffic("bp_kernel"),
                      "peak_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz "
                                    f"(median SM clock sampled during the timed region)",
                      "frac_of_max_clock_peak": round(bp_tflops / fp32_peak_max, 4),
                      "flops_per_pixel_pulse": FLOPS_PER_PIXEL_PULSE},
-        "roofline_rc": {"kernel": "rc_fused_kernel", "bound": "hbm", "achieved": round(rc_gbs, 1),
+        "roofline_rc": {"kernel": rc_name, "bound": "hbm", "achieved": round(rc_gbs, 1),
                         "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
                         "frac": round(rc_gbs / float(peaks.get("hbm_gbs", 6800.0)), 4),
-                        "traffic": kernel_traffic("rc_fused_kernel", os.path.join(src, "rc_kernel.cu")),
+                        "traffic": kernel_traffic(rc_name.split("<")[0]),
                         "peak_source": peak_src, "algorithmic_bytes_per_line": 8 * n_range * (1 + U)},
         "clocks": clk,
         "e2e": {"value": round(world * pp / e2e_s / 1e9, 3), "unit": UNIT,
@@ -239,9 +252,65 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": img_h.numel() * 8, "api": "sar_form_image_host"},
         "gpu_launches": launches,
     }
+    if not args.no_rc_sweep:
+        out["rc_sweep"] = rc_sweep(dev, peaks, reps=max(10, min(args.steps, 50)))
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(scene, budget_s=args.cpu_seconds)
     return out
+
+
+def rc_kernel_name(nr):
+    """The range-compression kernel the library launches for Nr-sample lines: the register-resident
+    radix-16 kernel for powers of two from 512 to 8192, the shared-memory mixed-radix one otherwise."""
+    return f"rc_reg_kernel<{nr}>" if nr >= 512 and nr & (nr - 1) == 0 else "rc_fused_kernel"
+
+
+def profile_case():
+    import torch
+    import domain_backprojection_gb300 as sar
+    import synth
+
+    scene = synth.make_scene(CONFIG_ID, device="cuda")
+    radar = scene["radar"]
+    plan = sar.sar_plan_create(radar, scene["grid"], 0)
+    sar.sar_plan_set_rc_layout(plan, sar.SAR_RC_POLYPHASE)
+    rc = torch.empty(radar.n_pulses, radar.n_range * radar.upsample, dtype=torch.complex64, device="cuda")
+    for _ in range(2):
+        sar.sar_range_compress(plan, scene["raw"], rc)
+        sar.sar_backproject(plan, rc, scene["pos"])
+    sar.sar_plan_sync(plan)
+    print(json.dumps({"profile_case": "ok", "workload": "spotlight 4096x4096 U=8, 1024x1024 image"}))
+
+
+def rc_sweep(dev, peaks, reps=20, n_sets=4):
+    """Range compression alone on the range-only workload: 4096 lines of Nr in {4096, 8192, 6000}
+    samples, U = 1, four rotating input sets; lines/s and fraction of the measured HBM bandwidth."""
+    import torch
+    import domain_backprojection_gb300 as sar
+    import synth
+
+    res = {}
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    for nr in synth.RC_SWEEP_NR:
+        scene = synth.make_rc_sweep(nr, n_lines=4096, device=dev)
+        plan = sar.sar_plan_create(scene["radar"], None, dev.index)
+        raws = [scene["raw"]] + [scene["raw"].clone() for _ in range(n_sets - 1)]
+        outs = [torch.empty_like(r) for r in raws]
+        for i in range(3):
+            sar.sar_range_compress(plan, raws[i % n_sets], outs[i % n_sets])
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(reps):
+            sar.sar_range_compress(plan, raws[i % n_sets], outs[i % n_sets])
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / reps
+        gbs = 4096 * 16 * nr / (ms * 1e-3) / 1e9
+        res[str(nr)] = {"kernel": rc_kernel_name(nr), "ms": round(ms, 4), "lines_per_s": round(4096 / (ms * 1e-3), 1), "gbs": round(gbs, 1),
+                        "frac_hbm": round(gbs / hbm, 4)}
+        del plan, raws, outs, scene
+    return res
 
 
 def cpu_baseline(scene, budget_s=12.0, threads=None):
@@ -316,8 +385,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rc-sweep", action="store_true")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="form two images of the spotlight scene (RC then BP, polyphase planes) and exit, untimed; "
+                         "the launch sequence profiler captures are taken on")
     args = ap.parse_args()
     rank, world, local_rank = rank_env()
+    if args.profile_case:
+        profile_case()
+        return
     if world > 1 and args.impl == "ours":
         import torch
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))

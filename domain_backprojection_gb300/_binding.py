@@ -69,6 +69,8 @@ def load_library(path: str):
         "sar_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "sar_plan_last_launches": ([P], I32),
         "sar_plan_set_rc_layout": ([P, ctypes.c_int], ctypes.c_int),
+        "sar_plan_set_timing": ([P, ctypes.c_int], ctypes.c_int),
+        "sar_plan_kernel_times": ([P, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -250,3 +252,18 @@ def sar_plan_set_rc_layout(plan: Plan, layout: int) -> None:
 
 def sar_plan_last_launches(plan: Plan) -> int:
     return int(lib().sar_plan_last_launches(plan.handle))
+
+
+def sar_plan_set_timing(plan: Plan, enable: bool = True) -> None:
+    """Record CUDA events around each later call's main kernel (see sar_plan_kernel_times)."""
+    _check(lib().sar_plan_set_timing(plan.handle, 1 if enable else 0), "sar_plan_set_timing")
+
+
+def sar_plan_kernel_times(plan: Plan) -> dict:
+    """Summed durations (ms) and call counts of the kernels recorded since timing was enabled or
+    last read: {"rc_ms", "rc_calls", "bp_ms", "bp_calls"}; the record is then cleared."""
+    rc_ms, bp_ms = ctypes.c_double(), ctypes.c_double()
+    rc_n, bp_n = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().sar_plan_kernel_times(plan.handle, ctypes.byref(rc_ms), ctypes.byref(rc_n), ctypes.byref(bp_ms),
+                                       ctypes.byref(bp_n)), "sar_plan_kernel_times")
+    return {"rc_ms": rc_ms.value, "rc_calls": rc_n.value, "bp_ms": bp_ms.value, "bp_calls": bp_n.value}

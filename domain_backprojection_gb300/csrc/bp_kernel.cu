@@ -288,7 +288,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // Per batch: issue the copies for batch b+1, prefetch the parameters of batch b+2, run the pixel
 // loop of batch b, then (one barrier later) turn the raw samples of b+1 into (tau, sigma) entries.
 template <int kTileX, bool kCheck, bool kPlanar>
-__global__ void __launch_bounds__(kBpThreads, 2) bp_kernel(BpArgs args)
+__global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs args)
 {
     constexpr int kTileY = kBpThreads * kBpRowsPerThread / kTileX;
     extern __shared__ float4 smem4[];
@@ -534,7 +534,8 @@ int bp_ctas_per_sm(int smem_bytes)
     return n > 0 ? n : 1;
 }
 
-cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s)
+cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s, cudaEvent_t main_begin,
+                      cudaEvent_t main_end)
 {
     if (a.pulse_end <= a.pulse_begin) return cudaSuccess;
     const int npulse = a.pulse_end - a.pulse_begin;
@@ -546,10 +547,12 @@ cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream
     if (pe != cudaSuccess) return pe;
     const dim3 grid(a.tiles_x, a.tiles_y, slices);
     const size_t smem = bp_smem_bytes(a);
+    if (main_begin && (pe = cudaEventRecord(main_begin, s)) != cudaSuccess) return pe;
     if (a.tile_w == 128) launch_bp_shape<128>(a, grid, smem, check_bounds, s);
     else if (a.tile_w == 64) launch_bp_shape<64>(a, grid, smem, check_bounds, s);
     else launch_bp_shape<32>(a, grid, smem, check_bounds, s);
     cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && main_end) e = cudaEventRecord(main_end, s);
     if (e != cudaSuccess || slices == 1) return e;
     const int64_t npix = (int64_t)a.nx * a.ny;
     const int blocks = (int)((npix + 255) / 256 < 4096 ? (npix + 255) / 256 : 4096);

@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "sar_internal.cuh"
@@ -32,6 +33,11 @@ struct sar_plan_s {
     // buffers for the host-pointer entry point (allocated on first use)
     void *d_raw = nullptr, *d_pos = nullptr, *d_rc = nullptr, *d_img = nullptr;
     int32_t last_launches = 0;
+    // kernel timing (sar_plan_set_timing): event pairs around the main kernel of each call
+    bool timing = false;
+    std::vector<cudaEvent_t> ev_pool;           // created on demand, destroyed with the plan
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev_rc, ev_bp;
+    size_t ev_used = 0;
 };
 
 namespace {
@@ -270,10 +276,10 @@ sar_status setup_bp(sar_plan p)
     a.wh = (int)std::ceil(rt / dr) + 3;
     a.w = 2 * a.wh + 1;
     a.min_range_tiles = (float)(100.0 * rt);
-    // 108 KB of shared memory per CTA (two per SM): 48 pulses' parameters, the rest for raw and staged
-    // rows; the kernel sizes its rows from the windows it actually stages
+    // 216 KB of shared memory per SM, split between the resident CTAs: 48 pulses' parameters, the
+    // rest for raw and staged rows; the kernel sizes its rows from the windows it actually stages
     a.pulses_per_batch = 48;
-    a.stage_bytes = 108 * 1024 - 15 * a.pulses_per_batch * (int)sizeof(float4);
+    a.stage_bytes = 216 * 1024 / sar::kBpCtasPerSm - 15 * a.pulses_per_batch * (int)sizeof(float4);
     if (a.w * 16 + ((a.w + 3) & ~1) * 8 > a.stage_bytes) return SAR_ERR_UNSUPPORTED;   // pixels too coarse
     a.err = p->d_err;
     {
@@ -303,9 +309,39 @@ sar_status setup_bp(sar_plan p)
     return SAR_OK;
 }
 
+constexpr size_t kMaxTimedCalls = 4096;     // per kind (range compression, backprojection)
+
+// The next free event pair of the plan's pool, or {null, null} when timing is off, the pool is
+// full or an event cannot be created (timing is best effort; the work is launched regardless).
+std::pair<cudaEvent_t, cudaEvent_t> timing_pair(sar_plan p, std::vector<std::pair<cudaEvent_t, cudaEvent_t>> &list)
+{
+    if (!p->timing || list.size() >= kMaxTimedCalls) return {nullptr, nullptr};
+    while (p->ev_pool.size() < p->ev_used + 2) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return {nullptr, nullptr};
+        p->ev_pool.push_back(e);
+    }
+    std::pair<cudaEvent_t, cudaEvent_t> pr{p->ev_pool[p->ev_used], p->ev_pool[p->ev_used + 1]};
+    p->ev_used += 2;
+    list.push_back(pr);
+    return pr;
+}
+
+// Launch range compression with the plan's timing events around it (when timing is on).
+sar_status timed_rc(sar_plan plan, const sar::RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines,
+                    cudaStream_t s)
+{
+    const auto ev = timing_pair(plan, plan->ev_rc);
+    if (ev.first && cudaEventRecord(ev.first, s) != cudaSuccess) return SAR_ERR_CUDA;
+    sar_status st = cuda_status(sar::launch_rc(a, raw, rc, n_lines, s));
+    if (st == SAR_OK && ev.second && cudaEventRecord(ev.second, s) != cudaSuccess) return SAR_ERR_CUDA;
+    return st;
+}
+
 void free_plan(sar_plan p)
 {
     if (!p) return;
+    for (cudaEvent_t e : p->ev_pool) cudaEventDestroy(e);
     cudaFree(p->d_tables);
     cudaFree(p->d_partial);
     cudaFree(p->d_table);
@@ -340,7 +376,8 @@ sar_status do_backproject(sar_plan plan, const void *rc, const double *pos, int3
     a.partial = plan->d_partial;
     a.planar = (layout == SAR_RC_POLYPHASE && plan->radar.upsample > 1) ? 1 : 0;
     plan->last_launches += slices > 1 ? 4 : 3;
-    return cuda_status(sar::launch_bp(a, slices, plan->check_bounds, s));
+    const auto ev = timing_pair(plan, plan->ev_bp);
+    return cuda_status(sar::launch_bp(a, slices, plan->check_bounds, s, ev.first, ev.second));
 }
 
 }  // namespace
@@ -431,8 +468,8 @@ sar_status sar_range_compress(sar_plan plan, const void *raw, void *rc, int64_t 
     plan->last_launches = 1;
     sar::RcArgs a = plan->rc;
     a.planar = plan->rc_layout == SAR_RC_POLYPHASE ? 1 : 0;
-    return cuda_status(sar::launch_rc(a, static_cast<const float2 *>(raw), static_cast<float2 *>(rc), n_lines,
-                                      static_cast<cudaStream_t>(stream)));
+    return timed_rc(plan, a, static_cast<const float2 *>(raw), static_cast<float2 *>(rc), n_lines,
+                    static_cast<cudaStream_t>(stream));
 }
 
 sar_status sar_backproject(sar_plan plan, const void *rc, const double *pos, int32_t pulse_begin,
@@ -466,8 +503,8 @@ sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, voi
     plan->last_launches = 1;
     sar::RcArgs ra = plan->rc;
     ra.planar = 1;
-    sar_status st = cuda_status(sar::launch_rc(ra, static_cast<const float2 *>(raw),
-                                               static_cast<float2 *>(workspace), plan->radar.n_pulses, s));
+    sar_status st = timed_rc(plan, ra, static_cast<const float2 *>(raw), static_cast<float2 *>(workspace),
+                             plan->radar.n_pulses, s);
     if (st != SAR_OK) return st;
     return do_backproject(plan, workspace, pos, 0, plan->radar.n_pulses, image, 0, s, SAR_RC_POLYPHASE);
 }
@@ -524,6 +561,38 @@ sar_status sar_plan_sync(sar_plan plan, void *stream)
 }
 
 int32_t sar_plan_last_launches(sar_plan plan) { return plan ? plan->last_launches : 0; }
+
+sar_status sar_plan_set_timing(sar_plan plan, int enable)
+{
+    if (!plan) return SAR_ERR_INVALID_ARG;
+    plan->timing = enable != 0;
+    return SAR_OK;
+}
+
+sar_status sar_plan_kernel_times(sar_plan plan, double *rc_ms, int32_t *rc_calls, double *bp_ms, int32_t *bp_calls)
+{
+    if (!plan || !rc_ms || !rc_calls || !bp_ms || !bp_calls) return SAR_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    sar_status st = SAR_OK;
+    auto sum = [&](std::vector<std::pair<cudaEvent_t, cudaEvent_t>> &list, double *ms, int32_t *n) {
+        double total = 0.0;
+        for (const auto &pr : list) {
+            float t = 0.0f;
+            cudaError_t e = cudaEventSynchronize(pr.second);
+            if (e == cudaSuccess) e = cudaEventElapsedTime(&t, pr.first, pr.second);
+            if (e != cudaSuccess) st = SAR_ERR_CUDA;
+            total += t;
+        }
+        *ms = total;
+        *n = (int32_t)list.size();
+        list.clear();
+    };
+    sum(plan->ev_rc, rc_ms, rc_calls);
+    sum(plan->ev_bp, bp_ms, bp_calls);
+    plan->ev_used = 0;
+    return st;
+}
 
 sar_status sar_plan_set_rc_layout(sar_plan plan, sar_rc_layout layout)
 {

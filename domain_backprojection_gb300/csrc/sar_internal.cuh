@@ -44,6 +44,7 @@ cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_
 constexpr int kBpRowsPerThread = 4;   // pixel rows each thread accumulates
 constexpr int kBpThreads = 512;        // threads per CTA: a tile of kBpThreads * kBpRowsPerThread pixels,
                                        // 128 x 16, 64 x 32 or 32 x 64 (x along azimuth), chosen per plan
+constexpr int kBpCtasPerSm = 2;        // resident CTAs per SM the kernel is built for (registers, shared memory)
 constexpr int kBpMaxSlices = 32;
 
 struct BpArgs {
@@ -89,6 +90,8 @@ struct BpArgs {
 size_t bp_smem_bytes(const BpArgs &a);
 cudaError_t bp_configure(int smem_bytes);
 int bp_ctas_per_sm(int smem_bytes);
-cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s);
+// main_begin / main_end (may be null): events recorded on s right around the pixel kernel
+cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s,
+                      cudaEvent_t main_begin = nullptr, cudaEvent_t main_end = nullptr);
 
 }  // namespace sar

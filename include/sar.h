@@ -169,6 +169,22 @@ const char *sar_status_string(sar_status status);
  * accounting in benchmarks); 0 for a NULL plan. */
 int32_t sar_plan_last_launches(sar_plan plan);
 
+/* Kernel timing, for benchmarks (no counterpart in the pages).  With enable != 0,
+ * each later range-compression call records a pair of CUDA events on its stream
+ * around the transform kernel, and each backprojection around the pixel kernel
+ * alone (not its small position-split, prep and reduction launches); at most
+ * 4096 calls of each kind are recorded until the next read.  The events belong
+ * to the plan.  enable = 0 stops recording.  Errors: SAR_ERR_INVALID_ARG for a
+ * NULL plan. */
+sar_status sar_plan_set_timing(sar_plan plan, int enable);
+
+/* Wait for the recorded events, then return the summed kernel durations in
+ * milliseconds and the number of calls recorded since timing was enabled or
+ * last read, for range compression (rc_*) and backprojection (bp_*), and forget
+ * them.  All four pointers are host pointers and must be non-NULL
+ * (SAR_ERR_INVALID_ARG otherwise); SAR_ERR_CUDA if an event could not be read. */
+sar_status sar_plan_kernel_times(sar_plan plan, double *rc_ms, int32_t *rc_calls, double *bp_ms, int32_t *bp_calls);
+
 #ifdef __cplusplus
 }
 #endif

@@ -57,6 +57,9 @@ def test_null_handles():
     assert L.sar_form_image_host(None, None, None, None, None) == 1
     assert L.sar_plan_sync(None, None) == 1
     assert L.sar_plan_last_launches(None) == 0
+    assert L.sar_plan_set_timing(None, 1) == 1
+    d, i = ctypes.c_double(), ctypes.c_int32()
+    assert L.sar_plan_kernel_times(None, ctypes.byref(d), ctypes.byref(i), ctypes.byref(d), ctypes.byref(i)) == 1
 
 
 @pytest.mark.parametrize("change,expect", [

@@ -201,3 +201,22 @@ def test_polyphase_layout_backprojection_matches_natural():
     assert rel_l2(img_pla.cpu().numpy(), ref) <= IMG_TOL
     L = sar.lib()
     assert L.sar_plan_set_rc_layout(plan.handle, 7) == 1
+
+
+def test_kernel_timing_records_each_call_and_leaves_results_unchanged():
+    s = synth.make_scene(1, device="cuda")
+    plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
+    want = sar.sar_form_image(plan, s["raw"], s["pos"])
+    sar.sar_plan_set_timing(plan, True)
+    got = [sar.sar_form_image(plan, s["raw"], s["pos"]) for _ in range(3)]
+    rc = sar.sar_range_compress(plan, s["raw"])
+    t = sar.sar_plan_kernel_times(plan)
+    assert t["rc_calls"] == 4 and t["bp_calls"] == 3
+    assert t["rc_ms"] > 0.0 and t["bp_ms"] > 0.0
+    assert all(torch.equal(g, want) for g in got)
+    assert rc.shape[0] == s["raw"].shape[0]
+    # read clears the record; timing off records nothing
+    sar.sar_plan_set_timing(plan, False)
+    sar.sar_form_image(plan, s["raw"], s["pos"])
+    t = sar.sar_plan_kernel_times(plan)
+    assert t == {"rc_ms": 0.0, "rc_calls": 0, "bp_ms": 0.0, "bp_calls": 0}
