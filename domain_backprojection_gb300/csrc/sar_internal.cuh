@@ -41,10 +41,10 @@ cudaError_t rc_configure(int n);
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s);
 
 // ----------------------------------------------------------- backprojection
-constexpr int kBpRowsPerThread = 4;   // pixel rows each thread accumulates
-constexpr int kBpThreads = 512;        // threads per CTA: a tile of kBpThreads * kBpRowsPerThread pixels,
+constexpr int kBpRowsPerThread = 8;   // pixel rows each thread accumulates
+constexpr int kBpThreads = 256;        // threads per CTA: a tile of kBpThreads * kBpRowsPerThread pixels,
                                        // 128 x 16, 64 x 32 or 32 x 64 (x along azimuth), chosen per plan
-constexpr int kBpCtasPerSm = 2;        // resident CTAs per SM the kernel is built for (registers, shared memory)
+constexpr int kBpCtasPerSm = 3;        // resident CTAs per SM the kernel is built for (registers, shared memory)
 constexpr int kBpMaxSlices = 32;
 
 struct BpArgs {
