@@ -202,7 +202,8 @@ __global__ void __launch_bounds__(512) rc_fused_kernel(const float2 *__restrict_
     extern __shared__ float4 smem4[];
     float2 *sm = reinterpret_cast<float2 *>(smem4);
     const int n = args.n, U = args.u;
-    float2 *Y = sm, *A = sm + n, *B = sm + 2 * n;
+    // U = 1 needs no copy of the spectrum: two buffers (see rc_smem_bytes)
+    float2 *A = sm, *B = sm + n, *Y = sm + 2 * n;
     const int un = U * n;
     const int lo_mask = (1 << args.ptw_lo_bits) - 1;
 
@@ -212,10 +213,22 @@ __global__ void __launch_bounds__(512) rc_fused_kernel(const float2 *__restrict_
         for (int i = threadIdx.x; i < n / 2; i += blockDim.x) reinterpret_cast<float4 *>(A)[i] = __ldg(src + i);
         __syncthreads();
         float2 *X = dft_forward(A, B, args);
+        float2 *out = rc + line * (int64_t)un;
+        if (U == 1) {
+            // conj(X H) in place, transformed, conjugated on the way out
+            for (int k = threadIdx.x; k < n; k += blockDim.x) X[k] = cconj(cmul(X[k], __ldg(args.h + k)));
+            __syncthreads();
+            const float2 *Z = dft_forward(X, X == A ? B : A, args);
+            for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
+                const float4 v = reinterpret_cast<const float4 *>(Z)[i];
+                reinterpret_cast<float4 *>(out)[i] = make_float4(v.x, -v.y, v.z, -v.w);
+            }
+            __syncthreads();
+            continue;
+        }
         // matched filter: Y = X * conj(DFT(chirp))
         for (int k = threadIdx.x; k < n; k += blockDim.x) Y[k] = cmul(X[k], __ldg(args.h + k));
         __syncthreads();
-        float2 *out = rc + line * (int64_t)un;
         for (int u = 0; u < U; u++) {
             // conj(Z_u)[k] = conj(Y[k]) * exp(-j 2 pi k_s u / (U Nr))
             for (int k = threadIdx.x; k < n; k += blockDim.x) {
@@ -231,22 +244,16 @@ __global__ void __launch_bounds__(512) rc_fused_kernel(const float2 *__restrict_
             }
             __syncthreads();
             float2 *Z = dft_forward(A, B, args);
-            // rc[U m + u] = conj(DFT(conj Z_u))[m] / Nr
-            if (U == 1) {
-                for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
-                    const float4 v = reinterpret_cast<const float4 *>(Z)[i];
-                    reinterpret_cast<float4 *>(out)[i] =
-                        make_float4(v.x * args.inv_n, -v.y * args.inv_n, v.z * args.inv_n, -v.w * args.inv_n);
-                }
-            } else if (args.planar) {
+            // rc[U m + u] = conj(DFT(conj Z_u))[m] (the 1 / Nr is in H)
+            if (args.planar) {
                 for (int m = threadIdx.x; m < n; m += blockDim.x) {
                     const float2 v = Z[m];
-                    out[(int64_t)u * n + m] = make_float2(v.x * args.inv_n, -v.y * args.inv_n);
+                    out[(int64_t)u * n + m] = cconj(v);
                 }
             } else {
                 for (int m = threadIdx.x; m < n; m += blockDim.x) {
                     const float2 v = Z[m];
-                    out[(int64_t)U * m + u] = make_float2(v.x * args.inv_n, -v.y * args.inv_n);
+                    out[(int64_t)U * m + u] = cconj(v);
                 }
             }
             __syncthreads();
@@ -358,7 +365,7 @@ __device__ __forceinline__ void reg_dft(float2 (&x)[16], float2 *buf, const floa
 }
 
 template <int N>
-__global__ void __launch_bounds__(N / 16) rc_reg_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc,
+__global__ void __launch_bounds__(N / 16, N == 4096 ? 2 : 1) rc_reg_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc,
                                                         int64_t n_lines, RcArgs args)
 {
     extern __shared__ float4 smem4[];
@@ -384,11 +391,11 @@ __global__ void __launch_bounds__(N / 16) rc_reg_kernel(const float2 *__restrict
             if (args.planar || U == 1) {
                 float2 *plane = out + (int64_t)u * N;
 #pragma unroll
-                for (int p = 0; p < 16; p++) plane[t + T * p] = make_float2(x[p].x * args.inv_n, -x[p].y * args.inv_n);
+                for (int p = 0; p < 16; p++) plane[t + T * p] = cconj(x[p]);
             } else {
 #pragma unroll
                 for (int p = 0; p < 16; p++)
-                    out[(int64_t)U * (t + T * p) + u] = make_float2(x[p].x * args.inv_n, -x[p].y * args.inv_n);
+                    out[(int64_t)U * (t + T * p) + u] = cconj(x[p]);
             }
             if (u + 1 < U) {
 #pragma unroll
@@ -405,13 +412,13 @@ size_t rc_reg_smem() { return (size_t)(N + N / 16) * sizeof(float2); }
 
 int rc_block_threads(int n) { return n >= 4096 ? 512 : 256; }
 
-size_t rc_smem_bytes(int n) { return (size_t)3 * n * sizeof(float2); }
+size_t rc_smem_bytes(int n, int u) { return (size_t)(u == 1 ? 2 : 3) * n * sizeof(float2); }
 
 cudaError_t rc_configure(int)
 {
     // the largest supported line (8192 samples) sets the limit, so plans of any size can coexist
     cudaError_t e = cudaFuncSetAttribute(rc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)rc_smem_bytes(8192));
+                                         (int)rc_smem_bytes(8192, 2));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(rc_reg_kernel<8192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)rc_reg_smem<8192>());
@@ -431,7 +438,7 @@ cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_
     case 2048: rc_reg_kernel<2048><<<grid, 2048 / 16, rc_reg_smem<2048>(), s>>>(raw, rc, n_lines, a); break;
     case 4096: rc_reg_kernel<4096><<<grid, 4096 / 16, rc_reg_smem<4096>(), s>>>(raw, rc, n_lines, a); break;
     case 8192: rc_reg_kernel<8192><<<grid, 8192 / 16, rc_reg_smem<8192>(), s>>>(raw, rc, n_lines, a); break;
-    default: rc_fused_kernel<<<grid, rc_block_threads(a.n), rc_smem_bytes(a.n), s>>>(raw, rc, n_lines, a); break;
+    default: rc_fused_kernel<<<grid, rc_block_threads(a.n), rc_smem_bytes(a.n, a.u), s>>>(raw, rc, n_lines, a); break;
     }
     return cudaGetLastError();
 }

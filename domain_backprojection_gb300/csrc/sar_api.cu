@@ -120,7 +120,7 @@ void build_matched_filter(const sar_radar &r, int n, std::vector<float2> &H)
             re += hre[j] * c - him[j] * s;
             im += hre[j] * s + him[j] * c;
         }
-        H[k] = make_float2((float)re, (float)-im);     // conjugate
+        H[k] = make_float2((float)(re / n), (float)(-im / n));     // conjugate, with the IDFT's 1 / Nr
     }
 }
 
@@ -153,7 +153,6 @@ sar_status setup_rc(sar_plan p)
     a.n = n;
     a.u = U;
     a.n_passes = plan_radices(n, a.radix);
-    a.inv_n = (float)(1.0 / n);
     int bits = 0;
     while ((1 << (2 * bits)) < un) bits++;                      // lo table ~ sqrt(U N) entries
     a.ptw_lo_bits = bits;

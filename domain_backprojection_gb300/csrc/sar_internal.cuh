@@ -25,8 +25,8 @@ struct RcArgs {
     int n_passes;            // Stockham passes of the Nr-point transform
     int radix[kMaxPasses];   // radix of each pass (product = Nr)
     int ptw_lo_bits;         // polyphase twiddle t = hi * 2^bits + lo
-    float inv_n;             // 1 / Nr (IDFT scaling: U * 1/(U Nr))
-    const float2 *h;         // matched filter spectrum H[k] = conj(DFT_N chirp)[k], natural order
+    const float2 *h;         // matched filter spectrum H[k] = conj(DFT_N chirp)[k] / Nr (the IDFT's
+                             // scaling U * 1/(U Nr) folded in), natural order
     const float2 *tw;        // w_N^t = exp(-2 pi i t / Nr), t in [0, Nr)
     const float2 *ptw_hi;    // exp(-2 pi i (hi << bits) / (U Nr))
     const float2 *ptw_lo;    // exp(-2 pi i lo / (U Nr)), lo < 2^bits
@@ -36,7 +36,7 @@ struct RcArgs {
 
 int rc_block_threads(int n);
 bool rc_has_reg_path(int n);
-size_t rc_smem_bytes(int n);
+size_t rc_smem_bytes(int n, int u);
 cudaError_t rc_configure(int n);
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s);
 

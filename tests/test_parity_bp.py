@@ -109,6 +109,29 @@ def test_grid_shapes(nx, ny):
     assert rel_l2(img.cpu().numpy(), ref) <= IMG_TOL
 
 
+@pytest.mark.parametrize("x_centre", [175.0, 1500.0])
+def test_squinted_grid(x_centre, monkeypatch):
+    # a grid off to the side of the track (squint up to ~15 degrees at x = 1500 m): the range
+    # gradient along azimuth is large, so neighbouring pixels of a warp read entries several bins
+    # apart and tile windows widen; both grids stay inside the compressed window
+    s = _small_case(48, 40, na=64)
+    g = s["grid"]
+    grid = dataclasses.replace(g, x0=x_centre - 0.5 * g.nx * g.dx)
+    plan = sar.sar_plan_create(s["radar"], grid, 0)
+    rc = sar.sar_range_compress(plan, s["raw"])
+    img = sar.sar_backproject(plan, rc, s["pos"])
+    sar.sar_plan_sync(plan)
+    ref = oracle.backproject(s["radar"], grid, rc.cpu().numpy(), s["pos"].cpu().numpy())
+    assert np.linalg.norm(ref) > 0.0
+    assert rel_l2(img.cpu().numpy(), ref) <= IMG_TOL
+    # the bounds-checked build finds every staged index inside its window on both paths
+    monkeypatch.setenv("SAR_CHECK_BOUNDS", "1")
+    checked = sar.sar_plan_create(s["radar"], grid, 0)
+    img_c = sar.sar_backproject(checked, rc, s["pos"])
+    sar.sar_plan_sync(checked)
+    assert rel_l2(img_c.cpu().numpy(), img.cpu().numpy()) <= 1e-6
+
+
 def test_window_edges_read_zero_outside_the_line():
     # a grid straddling the near and far ends of the compressed window: samples outside [0, U Nr) are zero
     s = _small_case(40, 40, na=32)
