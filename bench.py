@@ -40,6 +40,22 @@ def rank_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest of one float per rank over all ranks (the value itself for a single rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, seconds):
+    """Units per second of the whole job: every rank processes units_per_rank in `seconds` (the slowest
+    rank's time), so the job processes world * units_per_rank in that time (weak scaling)."""
+    return world * units_per_rank / seconds
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -183,13 +199,10 @@ def run_ours(args, rank, world, local_rank):
     assert kt["rc_calls"] == args.steps and kt["bp_calls"] == args.steps, kt
     rc_ms = kt["rc_ms"] / kt["rc_calls"]
     bp_ms = kt["bp_ms"] / kt["bp_calls"]
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
     pp = cfg.pixel_pulses
-    value = world * pp / (ms_step * 1e-3) / 1e9
+    value = whole_job_rate(pp, world, ms_step * 1e-3) / 1e9
 
     # end to end through the host-buffer entry point: H2D of raw + positions, both kernels, D2H of the image
     raw_h = scene["raw"].cpu().pin_memory()
@@ -203,10 +216,7 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(e2e_steps):
         sar.sar_form_image_host(plan, raw_h, pos_h, img_h)
     e2e_s = (time.perf_counter() - w0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, world, dev)
 
     if rank != 0:
         return None
@@ -231,8 +241,8 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "4 rotating input sets (536 MB raw) > 129 MB L2; 1.07 GB compressed lines per step",
                    "step": "sar_range_compress + sar_backproject with polyphase-plane compressed lines "
                            "(the kernels sar_form_image runs)"},
-        "rc_lines_per_s": round(world * cfg.n_pulses / (rc_ms * 1e-3), 1),
-        "bp_gpix_pulse_per_s": round(world * pp / (bp_ms * 1e-3) / 1e9, 3),
+        "rc_lines_per_s": round(whole_job_rate(cfg.n_pulses, world, rc_ms * 1e-3), 1),
+        "bp_gpix_pulse_per_s": round(whole_job_rate(pp, world, bp_ms * 1e-3) / 1e9, 3),
         "kernel_ms": {rc_name: round(rc_ms, 4), "bp_kernel": round(bp_ms, 4)},
         "roofline": {"kernel": "bp_kernel", "bound": "alu", "achieved": round(bp_tflops, 3),
                      "peak": round(fp32_peak, 3), "unit": "TFLOP/s", "frac": round(bp_tflops / fp32_peak, 4),
@@ -247,7 +257,7 @@ def run_ours(args, rank, world, local_rank):
                         "traffic": kernel_traffic(rc_name.split("<")[0]),
                         "peak_source": peak_src, "algorithmic_bytes_per_line": 8 * n_range * (1 + U)},
         "clocks": clk,
-        "e2e": {"value": round(world * pp / e2e_s / 1e9, 3), "unit": UNIT,
+        "e2e": {"value": round(whole_job_rate(pp, world, e2e_s) / 1e9, 3), "unit": UNIT,
                 "h2d_bytes_per_step": raw_h.numel() * 8 + pos_h.numel() * 8,
                 "d2h_bytes_per_step": img_h.numel() * 8, "api": "sar_form_image_host"},
         "gpu_launches": launches,
