@@ -1,6 +1,7 @@
 // sar_api.cu -- the C ABI declared in include/sar.h: plan creation (argument
 // validation, matched-filter and transform tables in float64 on the host),
 // range compression, backprojection and image formation entry points.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -32,6 +33,8 @@ struct sar_plan_s {
     int *h_err = nullptr;
     // buffers for the host-pointer entry point (allocated on first use)
     void *d_raw = nullptr, *d_pos = nullptr, *d_rc = nullptr, *d_img = nullptr;
+    cudaStream_t copy_stream = nullptr;    // host path: host-to-device copies, overlapped with compute
+    cudaEvent_t host_ev[5] = {};           // host path: call entry, then one per pulse chunk copied
     int32_t last_launches = 0;
     // kernel timing (sar_plan_set_timing): event pairs around the main kernel of each call
     bool timing = false;
@@ -341,6 +344,9 @@ void free_plan(sar_plan p)
 {
     if (!p) return;
     for (cudaEvent_t e : p->ev_pool) cudaEventDestroy(e);
+    for (cudaEvent_t e : p->host_ev)
+        if (e) cudaEventDestroy(e);
+    if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
     cudaFree(p->d_tables);
     cudaFree(p->d_partial);
     cudaFree(p->d_table);
@@ -527,13 +533,53 @@ sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double
     if (!plan->d_rc && e == cudaSuccess) e = cudaMalloc(&plan->d_rc, ws);
     if (!plan->d_img && e == cudaSuccess) e = cudaMalloc(&plan->d_img, img_bytes);
     if (e != cudaSuccess) return cuda_status(e);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = cudaMemcpyAsync(plan->d_raw, raw_host, raw_bytes, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(plan->d_pos, pos_host, pos_bytes, cudaMemcpyHostToDevice, s);
+    if (!plan->copy_stream && e == cudaSuccess) e = cudaStreamCreateWithFlags(&plan->copy_stream, cudaStreamNonBlocking);
+    for (cudaEvent_t &ev : plan->host_ev)
+        if (!ev && e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_status(e);
-    sar_status st = sar_form_image(plan, plan->d_raw, static_cast<const double *>(plan->d_pos), plan->d_img,
-                                   plan->d_rc, ws, stream);
-    if (st != SAR_OK) return st;
+    // Pulse chunks: the copy of chunk c + 1 runs on the plan's copy stream while chunk c is range
+    // compressed and backprojected (accumulating into the image) on the caller's stream.  The
+    // copy moves pulses several times faster than the kernels consume them, so the chunks grow
+    // (1/16, 3/16, 1/4 and 1/2 of the pulses): only the small first one is not overlapped.
+    cudaStream_t s = static_cast<cudaStream_t>(stream), cs = plan->copy_stream;
+    const int na = r.n_pulses;
+    int bounds[5] = {0, na, na, na, na};
+    int chunks = 1;
+    if (na >= 512) {
+        chunks = 4;
+        bounds[1] = na / 16;
+        bounds[2] = na / 4;
+        bounds[3] = na / 2;
+    }
+    const size_t line_bytes = (size_t)r.n_range * sizeof(float2);
+    e = cudaEventRecord(plan->host_ev[0], s);                   // earlier work on the caller's stream first
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, plan->host_ev[0], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(plan->d_pos, pos_host, pos_bytes, cudaMemcpyHostToDevice, cs);
+    for (int c = 0; c < chunks && e == cudaSuccess; c++) {
+        const int c0 = bounds[c], cnt = bounds[c + 1] - c0;
+        e = cudaMemcpyAsync(static_cast<char *>(plan->d_raw) + c0 * line_bytes,
+                            static_cast<const char *>(raw_host) + c0 * line_bytes, cnt * line_bytes,
+                            cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(plan->host_ev[1 + c], cs);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    sar::RcArgs ra = plan->rc;
+    ra.planar = 1;
+    int32_t launches = 0;
+    for (int c = 0; c < chunks; c++) {
+        const int c0 = bounds[c], cnt = bounds[c + 1] - c0;
+        e = cudaStreamWaitEvent(s, plan->host_ev[1 + c], 0);
+        if (e != cudaSuccess) return cuda_status(e);
+        float2 *rc = static_cast<float2 *>(plan->d_rc) + (size_t)c0 * r.n_range * r.upsample;
+        sar_status st = timed_rc(plan, ra, static_cast<const float2 *>(plan->d_raw) + (size_t)c0 * r.n_range, rc, cnt, s);
+        if (st != SAR_OK) return st;
+        plan->last_launches = 0;
+        st = do_backproject(plan, plan->d_rc, static_cast<const double *>(plan->d_pos), c0, cnt, plan->d_img, c > 0,
+                            s, SAR_RC_POLYPHASE);
+        if (st != SAR_OK) return st;
+        launches += 1 + plan->last_launches;
+    }
+    plan->last_launches = launches;
     e = cudaMemcpyAsync(image_host, plan->d_img, img_bytes, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return cuda_status(e);

@@ -122,9 +122,13 @@ sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, voi
 
 /* The same image formation from HOST buffers: copies raw and pos to device
  * buffers the plan owns (allocated on the first call), forms the image and
- * copies it back to image_host, then synchronises `stream`.  Host buffers
- * should be pinned for full copy bandwidth.  raw_host: [Na][Nr] complex64;
- * pos_host: [Na][3] float64; image_host: [ny][nx] complex64. */
+ * copies it back to image_host, then synchronises `stream`.  From 512 pulses on
+ * the pulses go in 4 growing chunks: while one is range compressed and backprojected on
+ * `stream` (accumulating into the image), the next is copied on a stream the
+ * plan owns, so the host-to-device copy overlaps the kernels.  The image then
+ * equals sar_form_image's up to the float32 summation order of the chunks.
+ * Host buffers should be pinned for full copy bandwidth.  raw_host: [Na][Nr]
+ * complex64; pos_host: [Na][3] float64; image_host: [ny][nx] complex64. */
 sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double *pos_host, void *image_host,
                                void *stream);
 
