@@ -123,6 +123,7 @@ KERNEL_SOURCES = {
     "bp_kernel": ["bp_kernel.cu", "sar_internal.cuh"],
     "rc_reg_kernel": ["rc_kernel.cu", "sar_internal.cuh"],
     "rc_fused_kernel": ["rc_kernel.cu", "sar_internal.cuh"],
+    "rc_mixed6000_kernel": ["rc_kernel.cu", "sar_internal.cuh"],
 }
 
 
@@ -271,8 +272,11 @@ def run_ours(args, rank, world, local_rank):
 
 def rc_kernel_name(nr):
     """The range-compression kernel the library launches for Nr-sample lines: the register-resident
-    radix-16 kernel for powers of two from 512 to 8192, the shared-memory mixed-radix one otherwise."""
-    return f"rc_reg_kernel<{nr}>" if nr >= 512 and nr & (nr - 1) == 0 else "rc_fused_kernel"
+    radix-16 kernel for powers of two from 512 to 8192, the register-resident radix-10/6 kernel for
+    6000, the shared-memory mixed-radix one otherwise."""
+    if nr >= 512 and nr <= 8192 and nr & (nr - 1) == 0:
+        return f"rc_reg_kernel<{nr}>"
+    return "rc_mixed6000_kernel" if nr == 6000 else "rc_fused_kernel"
 
 
 def profile_case():

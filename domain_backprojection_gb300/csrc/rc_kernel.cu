@@ -93,6 +93,47 @@ template <> struct Dft<5> {
     }
 };
 
+// 6 = 2 x 3 and 10 = 2 x 5: DFTs of the even and the odd samples, the odd ones turned by
+// exp(-2 pi i k / R), then sums and differences.
+template <> struct Dft<6> {
+    static __device__ __forceinline__ void run(float2 *a)
+    {
+        const float h = 0.86602540378443864676f;    // sin(2 pi / 6)
+        float2 e[3] = {a[0], a[2], a[4]};
+        float2 o[3] = {a[1], a[3], a[5]};
+        Dft<3>::run(e);
+        Dft<3>::run(o);
+        o[1] = cmul(o[1], make_float2(0.5f, -h));
+        o[2] = cmul(o[2], make_float2(-0.5f, -h));
+#pragma unroll
+        for (int k = 0; k < 3; k++) {
+            a[k] = cadd(e[k], o[k]);
+            a[k + 3] = csub(e[k], o[k]);
+        }
+    }
+};
+
+template <> struct Dft<10> {
+    static __device__ __forceinline__ void run(float2 *a)
+    {
+        const float c1 = 0.80901699437494742410f, s1 = 0.58778525229247312917f;   // 2 pi / 10
+        const float c2 = 0.30901699437494742410f, s2 = 0.95105651629515357212f;   // 4 pi / 10
+        float2 e[5] = {a[0], a[2], a[4], a[6], a[8]};
+        float2 o[5] = {a[1], a[3], a[5], a[7], a[9]};
+        Dft<5>::run(e);
+        Dft<5>::run(o);
+        o[1] = cmul(o[1], make_float2(c1, -s1));
+        o[2] = cmul(o[2], make_float2(c2, -s2));
+        o[3] = cmul(o[3], make_float2(-c2, -s2));
+        o[4] = cmul(o[4], make_float2(-c1, -s1));
+#pragma unroll
+        for (int k = 0; k < 5; k++) {
+            a[k] = cadd(e[k], o[k]);
+            a[k + 5] = csub(e[k], o[k]);
+        }
+    }
+};
+
 template <> struct Dft<8> {
     static __device__ __forceinline__ void run(float2 *a)
     {
@@ -408,6 +449,131 @@ __global__ void __launch_bounds__(N / 16, N == 4096 ? 2 : 1) rc_reg_kernel(const
 template <int N>
 size_t rc_reg_smem() { return (size_t)(N + N / 16) * sizeof(float2); }
 
+// ---------------------------------------------------------------------------
+// Register-resident transform for Nr = 6000 = 2^4 3 5^3 (the non-power-of-two
+// line of the range-only sweep): 200 threads of 30 elements, element t + T p in
+// slot p (T = 200), and four Stockham passes of radix 10, 10, 10 and 6, each
+// thread running 30 / R butterflies per pass.  As in the power-of-two kernel,
+// the first pass reads registers, the last leaves its output in registers in
+// the t + T p layout, and the passes in between exchange through shared memory.
+// ---------------------------------------------------------------------------
+template <int N, int E, int R, int L, bool kFirst, bool kLast>
+__device__ __forceinline__ void mixed_pass(float2 (&x)[E], float2 *buf, const float2 *__restrict__ tw)
+{
+    constexpr int T = N / E, SP = N / (L * R), NB = E / R;
+    static_assert(E % R == 0 && N % (L * R) == 0, "pass does not fit the layout");
+    const int t = threadIdx.x;
+    if (kFirst) {
+        // butterfly i takes elements (t + T i) + (N / R) p = t + T (i + NB p): slot i + NB p
+        float2 y[E];
+#pragma unroll
+        for (int i = 0; i < NB; i++)
+#pragma unroll
+            for (int p = 0; p < R; p++) y[i * R + p] = x[i + NB * p];
+#pragma unroll
+        for (int k = 0; k < E; k++) x[k] = y[k];
+    } else {
+#pragma unroll
+        for (int i = 0; i < NB; i++) {
+            const int b = t + T * i;
+            const int jp = b % SP, kp = b / SP;
+#pragma unroll
+            for (int p = 0; p < R; p++) x[i * R + p] = buf[kp * SP * R + jp + SP * p];
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < NB; i++) {
+        const int b = t + T * i;
+        const int jp = b % SP, kp = b / SP;
+        if (!kFirst) {
+            float2 w[R];
+            twiddle_powers<R>(__ldg(tw + SP * kp), w);
+#pragma unroll
+            for (int p = 1; p < R; p++) x[i * R + p] = cmul(x[i * R + p], w[p]);
+        }
+        Dft<R>::run(x + i * R);
+        if (!kLast) {
+#pragma unroll
+            for (int q = 0; q < R; q++) buf[(kp + L * q) * SP + jp] = x[i * R + q];
+        }
+    }
+    if (!kLast) __syncthreads();
+    if (kLast) {
+        // outputs (t + T i) + (N / R) q = t + T (i + NB q): slot i + NB q
+        float2 y[E];
+#pragma unroll
+        for (int i = 0; i < NB; i++)
+#pragma unroll
+            for (int q = 0; q < R; q++) y[i + NB * q] = x[i * R + q];
+#pragma unroll
+        for (int k = 0; k < E; k++) x[k] = y[k];
+    }
+}
+
+// Forward DFT of the 6000-point line held as x[p] = element t + T p; result in the same layout.
+__device__ __forceinline__ void mixed_dft6000(float2 (&x)[30], float2 *buf, const float2 *__restrict__ tw)
+{
+    mixed_pass<6000, 30, 10, 1, true, false>(x, buf, tw);
+    mixed_pass<6000, 30, 10, 10, false, false>(x, buf, tw);
+    mixed_pass<6000, 30, 10, 100, false, false>(x, buf, tw);
+    mixed_pass<6000, 30, 6, 1000, false, true>(x, buf, tw);
+    __syncthreads();                                            // the buffer is free for the next transform
+}
+
+constexpr int kRcMixedCtas = 1;     // the 30-element layout wants ~250 registers; bounding them to fit
+                                    // 2 CTAs per SM spills and runs slower at U = 8
+
+template <bool kMulti>
+__global__ void __launch_bounds__(200, kRcMixedCtas) rc_mixed6000_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc,
+                                                           int64_t n_lines, RcArgs args)
+{
+    constexpr int N = 6000, E = 30, T = N / E;
+    extern __shared__ float4 smem4[];
+    float2 *buf = reinterpret_cast<float2 *>(smem4);
+    const int t = threadIdx.x;
+    const int U = kMulti ? args.u : 1;
+    for (int64_t line = blockIdx.x; line < n_lines; line += gridDim.x) {
+        float2 x[E];
+        const float2 *src = raw + line * N;
+#pragma unroll
+        for (int p = 0; p < E; p++) x[p] = __ldg(src + t + T * p);
+        mixed_dft6000(x, buf, args.tw);
+        // matched filter (with the IDFT's 1 / Nr)
+#pragma unroll
+        for (int p = 0; p < E; p++) x[p] = cmul(x[p], __ldg(args.h + t + T * p));
+        float2 *out = rc + line * (int64_t)(U * N);
+        if constexpr (!kMulti) {
+#pragma unroll
+            for (int p = 0; p < E; p++) x[p] = cconj(x[p]);
+            mixed_dft6000(x, buf, args.tw);
+#pragma unroll
+            for (int p = 0; p < E; p++) out[t + T * p] = cconj(x[p]);
+            continue;
+        }
+        float2 y[E];
+#pragma unroll
+        for (int p = 0; p < E; p++) y[p] = x[p];
+        for (int u = 0; u < U; u++) {
+#pragma unroll
+            for (int p = 0; p < E; p++) x[p] = cconj(y[p]);
+            mixed_dft6000(x, buf, args.tw);
+            if (args.planar) {
+                float2 *plane = out + (int64_t)u * N;
+#pragma unroll
+                for (int p = 0; p < E; p++) plane[t + T * p] = cconj(x[p]);
+            } else {
+#pragma unroll
+                for (int p = 0; p < E; p++) out[(int64_t)U * (t + T * p) + u] = cconj(x[p]);
+            }
+            if (u + 1 < U) {
+#pragma unroll
+                for (int p = 0; p < E; p++) y[p] = cmul(y[p], __ldg(args.ramp + t + T * p));
+            }
+        }
+    }
+}
+
 }  // namespace
 
 int rc_block_threads(int n) { return n >= 4096 ? 512 : 256; }
@@ -438,6 +604,10 @@ cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_
     case 2048: rc_reg_kernel<2048><<<grid, 2048 / 16, rc_reg_smem<2048>(), s>>>(raw, rc, n_lines, a); break;
     case 4096: rc_reg_kernel<4096><<<grid, 4096 / 16, rc_reg_smem<4096>(), s>>>(raw, rc, n_lines, a); break;
     case 8192: rc_reg_kernel<8192><<<grid, 8192 / 16, rc_reg_smem<8192>(), s>>>(raw, rc, n_lines, a); break;
+    case 6000:
+        if (a.u == 1) rc_mixed6000_kernel<false><<<grid, 200, 6000 * sizeof(float2), s>>>(raw, rc, n_lines, a);
+        else rc_mixed6000_kernel<true><<<grid, 200, 6000 * sizeof(float2), s>>>(raw, rc, n_lines, a);
+        break;
     default: rc_fused_kernel<<<grid, rc_block_threads(a.n), rc_smem_bytes(a.n, a.u), s>>>(raw, rc, n_lines, a); break;
     }
     return cudaGetLastError();
