@@ -36,6 +36,10 @@ def lib():
         L.or_chirp_count.restype = ctypes.c_int32
         L.or_matched_filter.argtypes = [P, ctypes.c_int32, P]
         L.or_range_compress.argtypes = [P, P, ctypes.c_int64, P, ctypes.c_int]
+        L.or_window.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_double, P]
+        L.or_matched_filter_w.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_double, P]
+        L.or_range_compress_w.argtypes = [P, P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_double, P,
+                                          ctypes.c_int]
         L.or_backproject.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int64, P,
                                      ctypes.c_int, ctypes.c_int]
         L.or_max_threads.restype = ctypes.c_int
@@ -67,21 +71,33 @@ def chirp_count(radar):
     return int(lib().or_chirp_count(ctypes.byref(_radar(radar))))
 
 
-def matched_filter(radar, n=None):
+WINDOW_NONE, WINDOW_HAMMING, WINDOW_TAYLOR = 0, 1, 2
+
+
+def window(kind, nc, nbar=4, sll_db=35.0):
+    """The nc range weights of the reference chirp (kind: WINDOW_NONE / _HAMMING / _TAYLOR)."""
+    w = np.zeros(nc, dtype=np.float64)
+    lib().or_window(int(kind), int(nc), int(nbar), float(sll_db), _ptr(w))
+    return w
+
+
+def matched_filter(radar, n=None, window=WINDOW_NONE, nbar=4, sll_db=35.0):
     n = radar.n_range if n is None else n
     H = np.zeros(n, dtype=np.complex128)
-    lib().or_matched_filter(ctypes.byref(_radar(radar, n_range=n)), n, _ptr(H))
+    lib().or_matched_filter_w(ctypes.byref(_radar(radar, n_range=n)), n, int(window), int(nbar), float(sll_db),
+                              _ptr(H))
     return H
 
 
-def range_compress(radar, raw, upsample=None, threads=0):
-    """raw [lines][N] complex64 -> rc [lines][U N] complex128."""
+def range_compress(radar, raw, upsample=None, threads=0, window=WINDOW_NONE, nbar=4, sll_db=35.0):
+    """raw [lines][N] complex64 -> rc [lines][U N] complex128 (matched filter weighted by `window`)."""
     raw = np.ascontiguousarray(raw, dtype=np.complex64)
     lines, n = raw.shape
     U = radar.upsample if upsample is None else upsample
     r = _radar(radar, upsample=U, n_range=n)
     rc = np.zeros((lines, U * n), dtype=np.complex128)
-    lib().or_range_compress(ctypes.byref(r), _ptr(raw), lines, _ptr(rc), int(threads))
+    lib().or_range_compress_w(ctypes.byref(r), _ptr(raw), lines, int(window), int(nbar), float(sll_db), _ptr(rc),
+                              int(threads))
     return rc
 
 

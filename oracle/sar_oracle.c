@@ -141,38 +141,92 @@ int32_t or_chirp_count(const or_radar *r)
     return (int32_t)(fabs(x - k) < 1e-6 ? k : floor(x));
 }
 
+/* Range weighting of the reference chirp ("GPU-accelerated backprojection
+ * SAR imaging", section 3.1: an unweighted matched filter leaves range
+ * sidelobes of about -13 dB; Hamming or Taylor weighting lowers them and widens
+ * the main lobe).  Reading: the weight multiplies the nc samples of the
+ * reference chirp in time, sample i = s - s_first in [0, nc).
+ *   kind 0: none, w = 1;
+ *   kind 1: Hamming, w = 0.54 - 0.46 cos(2 pi i / (nc - 1));
+ *   kind 2: Taylor with nbar terms and peak sidelobes sll_db below the peak
+ *     (Taylor's line-source distribution sampled at the chirp samples):
+ *     A = acosh(10^(sll_db / 20)) / pi,  sigma^2 = nbar^2 / (A^2 + (nbar - 1/2)^2),
+ *     F_m = (-1)^(m+1) / 2 * prod_{n=1}^{nbar-1} (1 - m^2 / (sigma^2 (A^2 + (n - 1/2)^2)))
+ *                          / prod_{n=1, n != m}^{nbar-1} (1 - m^2 / n^2),   m = 1 .. nbar - 1,
+ *     w = 1 + 2 sum_m F_m cos(2 pi m x),  x = (i - (nc - 1) / 2) / nc.
+ * Writes nc weights. */
+void or_window(int32_t kind, int32_t nc, int32_t nbar, double sll_db, double *w)
+{
+    for (int32_t i = 0; i < nc; i++) w[i] = 1.0;
+    if (kind == 1) {
+        for (int32_t i = 0; i < nc; i++) w[i] = 0.54 - 0.46 * cos(2.0 * M_PI * i / (double)(nc - 1));
+    } else if (kind == 2) {
+        const double A = acosh(pow(10.0, sll_db / 20.0)) / M_PI;
+        const double sig2 = (double)nbar * nbar / (A * A + (nbar - 0.5) * (nbar - 0.5));
+        double *F = calloc((size_t)(nbar > 1 ? nbar : 1), sizeof(double));
+        for (int32_t m = 1; m < nbar; m++) {
+            double num = 1.0, den = 1.0;
+            for (int32_t k = 1; k < nbar; k++) {
+                num *= 1.0 - (double)m * m / (sig2 * (A * A + (k - 0.5) * (k - 0.5)));
+                if (k != m) den *= 1.0 - (double)m * m / ((double)k * k);
+            }
+            F[m] = ((m % 2) ? 0.5 : -0.5) * num / den;
+        }
+        for (int32_t i = 0; i < nc; i++) {
+            const double x = (i - 0.5 * (nc - 1)) / nc;
+            double v = 1.0;
+            for (int32_t m = 1; m < nbar; m++) v += 2.0 * F[m] * cos(2.0 * M_PI * m * x);
+            w[i] = v;
+        }
+        free(F);
+    }
+}
+
 /* The reference chirp h on an N-point circular line (centred on index 0),
- * then H = conj(DFT_N h).  Writes N complex values. */
-void or_matched_filter(const or_radar *r, int32_t n, double *H_out)
+ * weighted by or_window(kind, ...), then H = conj(DFT_N h).  Writes N complex
+ * values. */
+void or_matched_filter_w(const or_radar *r, int32_t n, int32_t kind, int32_t nbar, double sll_db, double *H_out)
 {
     cplx *h = calloc((size_t)n, sizeof(cplx));
     double K = r->bandwidth / r->pulse_width;
     int32_t nc = or_chirp_count(r);
-    /* integer sample offsets s with -nc/2 <= s < nc/2 */
+    double *w = malloc(sizeof(double) * (size_t)nc);
+    or_window(kind, nc, nbar, sll_db, w);
+    /* integer sample offsets s with -nc/2 <= s < nc/2; the first is s_first = -floor(nc / 2) */
+    const int64_t s_first = -(int64_t)(nc / 2);
     for (int64_t s = -(int64_t)n; s <= (int64_t)n; s++) {
         if (2 * s < -nc || 2 * s >= nc) continue;
         double tau = (double)s / r->fs;
         int64_t idx = ((s % n) + n) % n;
-        h[idx] = cexp(I * M_PI * K * tau * tau);
+        h[idx] = w[s - s_first] * cexp(I * M_PI * K * tau * tau);
     }
     or_dft((double *)h, n, -1);
     cplx *H = (cplx *)H_out;
     for (int32_t k = 0; k < n; k++) H[k] = conj(h[k]);
+    free(w);
     free(h);
+}
+
+/* The unweighted matched filter. */
+void or_matched_filter(const or_radar *r, int32_t n, double *H_out)
+{
+    or_matched_filter_w(r, n, 0, 0, 0.0, H_out);
 }
 
 /* ------------------------------------------------- range compression ---- */
 
 /* Range-compress n_lines lines of raw [n_lines][N] complex64 into
- * rc [n_lines][U N] complex128:
+ * rc [n_lines][U N] complex128 with the matched filter weighted by
+ * or_window(kind, ...):
  *   X = DFT_N(s); Y = X H; Y' = zero-pad of Y to U N points (bins with
  *   2k >= N at the top end); rc = U * IDFT_{UN}(Y') with IDFT's 1/(U N).  */
-void or_range_compress(const or_radar *r, const float *raw, int64_t n_lines, double *rc_out, int threads)
+void or_range_compress_w(const or_radar *r, const float *raw, int64_t n_lines, int32_t kind, int32_t nbar,
+                         double sll_db, double *rc_out, int threads)
 {
     const int32_t n = r->n_range, U = r->upsample;
     const int64_t un = (int64_t)U * n;
     cplx *H = malloc(sizeof(cplx) * (size_t)n);
-    or_matched_filter(r, n, (double *)H);
+    or_matched_filter_w(r, n, kind, nbar, sll_db, (double *)H);
 #ifdef _OPENMP
     if (threads > 0) omp_set_num_threads(threads);
 #pragma omp parallel for schedule(dynamic, 1)
@@ -194,6 +248,12 @@ void or_range_compress(const or_radar *r, const float *raw, int64_t n_lines, dou
         free(X); free(Yp);
     }
     free(H);
+}
+
+/* Unweighted range compression. */
+void or_range_compress(const or_radar *r, const float *raw, int64_t n_lines, double *rc_out, int threads)
+{
+    or_range_compress_w(r, raw, n_lines, 0, 0, 0.0, rc_out, threads);
 }
 
 /* ------------------------------------------------------- backprojection ---- */

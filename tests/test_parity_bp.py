@@ -255,3 +255,31 @@ def test_kernel_timing_records_each_call_and_leaves_results_unchanged():
     sar.sar_form_image(plan, s["raw"], s["pos"])
     t = sar.sar_plan_kernel_times(plan)
     assert t == {"rc_ms": 0.0, "rc_calls": 0, "bp_ms": 0.0, "bp_calls": 0}
+
+
+def test_form_image_captures_into_a_cuda_graph():
+    # sar_form_image enqueues its launches with no allocation or synchronisation, so a caller can
+    # capture it into a CUDA graph and replay it on new echoes copied into the captured buffers
+    s = synth.make_scene(1, device="cuda")
+    plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
+    raw = s["raw"].clone()
+    pos = s["pos"].clone()
+    ws = torch.empty(sar.sar_workspace_size(plan), dtype=torch.uint8, device="cuda")
+    img = torch.empty(s["grid"].ny, s["grid"].nx, dtype=torch.complex64, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        sar.sar_form_image(plan, raw, pos, image=img, workspace=ws)      # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sar.sar_form_image(plan, raw, pos, image=img, workspace=ws)
+    other = synth.make_scene(dataclasses.replace(synth.CONFIGS[1], seed=91), device="cuda")
+    for scene in (s, other):
+        raw.copy_(scene["raw"])
+        pos.copy_(scene["pos"])
+        g.replay()
+        want = sar.sar_form_image(plan, scene["raw"], scene["pos"])
+        torch.cuda.synchronize()
+        assert torch.equal(img, want)
+    sar.sar_plan_sync(plan)
