@@ -70,6 +70,7 @@ def load_library(path: str):
         "sar_plan_last_launches": ([P], I32),
         "sar_plan_set_rc_layout": ([P, ctypes.c_int], ctypes.c_int),
         "sar_plan_set_timing": ([P, ctypes.c_int], ctypes.c_int),
+        "sar_plan_set_range_window": ([P, ctypes.c_int, I32, ctypes.c_double], ctypes.c_int),
         "sar_plan_kernel_times": ([P, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -267,3 +268,12 @@ def sar_plan_kernel_times(plan: Plan) -> dict:
     _check(lib().sar_plan_kernel_times(plan.handle, ctypes.byref(rc_ms), ctypes.byref(rc_n), ctypes.byref(bp_ms),
                                        ctypes.byref(bp_n)), "sar_plan_kernel_times")
     return {"rc_ms": rc_ms.value, "rc_calls": rc_n.value, "bp_ms": bp_ms.value, "bp_calls": bp_n.value}
+
+
+SAR_WINDOW_NONE, SAR_WINDOW_HAMMING, SAR_WINDOW_TAYLOR = 0, 1, 2
+
+
+def sar_plan_set_range_window(plan: Plan, window: int, taylor_nbar: int = 4, taylor_sll_db: float = 35.0) -> None:
+    """Weight the plan's matched filter: SAR_WINDOW_NONE, SAR_WINDOW_HAMMING or SAR_WINDOW_TAYLOR."""
+    _check(lib().sar_plan_set_range_window(plan.handle, int(window), int(taylor_nbar), float(taylor_sll_db)),
+           "sar_plan_set_range_window")

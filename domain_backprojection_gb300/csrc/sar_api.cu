@@ -99,19 +99,56 @@ sar_status cuda_status(cudaError_t e)
 // The matched-filter spectrum conj(DFT_N(h)), h the centred up-chirp on the
 // integer samples s with -nc/2 <= s < nc/2, stored circularly; the DFT is a
 // direct sum over the nc nonzero samples, in float64.
-void build_matched_filter(const sar_radar &r, int n, std::vector<float2> &H)
+// Weights of the nc reference-chirp samples ("GPU-accelerated backprojection SAR imaging",
+// section 3.1: weighting the matched filter trades the ~-13 dB range sidelobes of the unweighted
+// one for a wider main lobe).  Hamming: 0.54 - 0.46 cos(2 pi i / (nc - 1)).  Taylor (nbar terms,
+// sidelobes sll_db below the peak): the line-source distribution 1 + 2 sum_m F_m cos(2 pi m x) at
+// x = (i - (nc - 1) / 2) / nc, with A = acosh(10^(sll/20)) / pi, sigma^2 = nbar^2 / (A^2 +
+// (nbar - 1/2)^2) and F_m = (-1)^(m+1)/2 prod_n (1 - m^2 / (sigma^2 (A^2 + (n - 1/2)^2))) /
+// prod_{n != m} (1 - m^2 / n^2), n = 1 .. nbar - 1.
+std::vector<double> range_weights(int kind, int nc, int nbar, double sll_db)
+{
+    std::vector<double> w((size_t)nc, 1.0);
+    if (kind == SAR_WINDOW_HAMMING) {
+        for (int i = 0; i < nc; i++) w[i] = 0.54 - 0.46 * std::cos(2.0 * M_PI * i / (nc - 1));
+    } else if (kind == SAR_WINDOW_TAYLOR) {
+        const double A = std::acosh(std::pow(10.0, sll_db / 20.0)) / M_PI;
+        const double s2 = nbar * (double)nbar / (A * A + (nbar - 0.5) * (nbar - 0.5));
+        std::vector<double> F((size_t)nbar, 0.0);
+        for (int m = 1; m < nbar; m++) {
+            double num = 1.0, den = 1.0;
+            for (int k = 1; k < nbar; k++) {
+                num *= 1.0 - m * (double)m / (s2 * (A * A + (k - 0.5) * (k - 0.5)));
+                if (k != m) den *= 1.0 - m * (double)m / (k * (double)k);
+            }
+            F[m] = (m % 2 ? 0.5 : -0.5) * num / den;
+        }
+        for (int i = 0; i < nc; i++) {
+            const double x = (i - 0.5 * (nc - 1)) / nc;
+            double v = 1.0;
+            for (int m = 1; m < nbar; m++) v += 2.0 * F[m] * std::cos(2.0 * M_PI * m * x);
+            w[i] = v;
+        }
+    }
+    return w;
+}
+
+void build_matched_filter(const sar_radar &r, int n, std::vector<float2> &H, int window = SAR_WINDOW_NONE,
+                          int nbar = 4, double sll_db = 35.0)
 {
     const int nc = chirp_samples(r);
     const double K = r.bandwidth / r.pulse_width;
+    const std::vector<double> w = range_weights(window, nc, nbar, sll_db);
     std::vector<double> hre, him;
     std::vector<int> hs;
     for (int s = -nc; s <= nc; s++) {
         if (2 * s < -nc || 2 * s >= nc) continue;
         const double tau = s / r.fs;
         const double ph = M_PI * K * tau * tau;
+        const double a = w[(size_t)(s + nc / 2)];                 // sample s - s_first, s_first = -(nc / 2)
         hs.push_back(((s % n) + n) % n);
-        hre.push_back(std::cos(ph));
-        him.push_back(std::sin(ph));
+        hre.push_back(a * std::cos(ph));
+        him.push_back(a * std::sin(ph));
     }
     H.resize(n);
     for (int k = 0; k < n; k++) {
@@ -606,6 +643,24 @@ sar_status sar_plan_sync(sar_plan plan, void *stream)
 }
 
 int32_t sar_plan_last_launches(sar_plan plan) { return plan ? plan->last_launches : 0; }
+
+sar_status sar_plan_set_range_window(sar_plan plan, sar_window window, int32_t taylor_nbar, double taylor_sll_db)
+{
+    if (!plan) return SAR_ERR_INVALID_ARG;
+    if (window != SAR_WINDOW_NONE && window != SAR_WINDOW_HAMMING && window != SAR_WINDOW_TAYLOR)
+        return SAR_ERR_INVALID_ARG;
+    if (window == SAR_WINDOW_TAYLOR &&
+        (taylor_nbar < 2 || taylor_nbar > 64 || !(taylor_sll_db > 0.0) || !(taylor_sll_db <= 120.0)))
+        return SAR_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    std::vector<float2> H;
+    build_matched_filter(plan->radar, plan->radar.n_range, H, window, taylor_nbar, taylor_sll_db);
+    // work already queued on any stream may still read the old filter
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(plan->d_tables, H.data(), H.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    return cuda_status(e);
+}
 
 sar_status sar_plan_set_timing(sar_plan plan, int enable)
 {

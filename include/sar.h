@@ -173,6 +173,24 @@ const char *sar_status_string(sar_status status);
  * accounting in benchmarks); 0 for a NULL plan. */
 int32_t sar_plan_last_launches(sar_plan plan);
 
+/* Range weighting of the matched filter ("GPU-accelerated backprojection SAR
+ * imaging", section 3.1: the unweighted filter leaves range sidelobes of about
+ * -13 dB; weighting lowers them and widens the main lobe 1.3-1.5 times).  The
+ * weight multiplies the Nchirp samples i = 0 .. Nchirp-1 of the reference chirp:
+ *   SAR_WINDOW_NONE     w = 1 (the plan's default);
+ *   SAR_WINDOW_HAMMING  w = 0.54 - 0.46 cos(2 pi i / (Nchirp - 1));
+ *   SAR_WINDOW_TAYLOR   Taylor's distribution with taylor_nbar terms and peak
+ *                       sidelobes taylor_sll_db below the main lobe, sampled at
+ *                       x = (i - (Nchirp - 1)/2) / Nchirp (e.g. nbar 4, 35 dB). */
+typedef enum { SAR_WINDOW_NONE = 0, SAR_WINDOW_HAMMING = 1, SAR_WINDOW_TAYLOR = 2 } sar_window;
+
+/* Rebuild the plan's matched filter with `window` (taylor_* are read for
+ * SAR_WINDOW_TAYLOR only: 2 <= taylor_nbar <= 64, 0 < taylor_sll_db <= 120;
+ * SAR_ERR_INVALID_ARG otherwise).  Synchronises the device first, so that work
+ * already queued keeps the filter it was queued with; later range compressions
+ * (and image formations) use the new one.  SAR_ERR_CUDA if the upload fails. */
+sar_status sar_plan_set_range_window(sar_plan plan, sar_window window, int32_t taylor_nbar, double taylor_sll_db);
+
 /* Kernel timing, for benchmarks (no counterpart in the pages).  With enable != 0,
  * each later range-compression call records a pair of CUDA events on its stream
  * around the transform kernel, and each backprojection around the pixel kernel

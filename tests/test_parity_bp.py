@@ -283,3 +283,18 @@ def test_form_image_captures_into_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(img, want)
     sar.sar_plan_sync(plan)
+
+
+def test_form_image_with_range_weighting():
+    # Hamming-weighted range compression through sar_form_image against the oracle's weighted image
+    s = synth.make_scene(1, device="cuda")
+    plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
+    sar.sar_plan_set_range_window(plan, sar.SAR_WINDOW_HAMMING)
+    img = sar.sar_form_image(plan, s["raw"], s["pos"])
+    sar.sar_plan_sync(plan)
+    rc = oracle.range_compress(s["radar"], s["raw"].cpu().numpy(), threads=ORACLE_THREADS,
+                               window=oracle.WINDOW_HAMMING)
+    ref = oracle.backproject(s["radar"], s["grid"], rc, s["pos"].cpu().numpy(), threads=ORACLE_THREADS)
+    assert rel_l2(img.cpu().numpy(), ref) <= IMG_TOL
+    centres = target_pixels(s)
+    check_peaks(img.cpu().numpy(), ref, s["grid"], centres, 6)

@@ -115,3 +115,33 @@ def test_rc_polyphase_layout(n, U):
     assert np.array_equal(pla, nat)
     ref = oracle.range_compress(radar, raw.numpy(), threads=ORACLE_THREADS).reshape(5, n, U).transpose(0, 2, 1)
     assert rel_l2(pla, ref) <= RC_TOL
+
+
+@pytest.mark.parametrize("window,nbar,sll", [(sar.SAR_WINDOW_HAMMING, 4, 35.0), (sar.SAR_WINDOW_TAYLOR, 4, 35.0),
+                                             (sar.SAR_WINDOW_TAYLOR, 6, 40.0)])
+@pytest.mark.parametrize("n,U,lines", [(4096, 8, 6), (6000, 1, 20), (1000, 2, 5), (1024, 4, 8)])
+def test_rc_range_window(window, nbar, sll, n, U, lines):
+    # the weighted matched filter ("GPU-accelerated backprojection SAR imaging", section 3.1)
+    radar = synth.Radar(range_start=5000.0, n_pulses=lines, n_range=n, upsample=U)
+    raw = _noise(lines, n, n + 7 * U + window)
+    plan = sar.sar_plan_create(radar, None, 0)
+    sar.sar_plan_set_range_window(plan, window, nbar, sll)
+    got = sar.sar_range_compress(plan, raw.cuda()).cpu().numpy()
+    ref = oracle.range_compress(radar, raw.numpy(), threads=ORACLE_THREADS, window=window, nbar=nbar, sll_db=sll)
+    for i in range(lines):
+        assert rel_l2(got[i], ref[i]) <= RC_TOL, f"line {i}"
+    # back to the unweighted filter
+    sar.sar_plan_set_range_window(plan, sar.SAR_WINDOW_NONE, 0, 0.0)
+    got0 = sar.sar_range_compress(plan, raw.cuda()).cpu().numpy()
+    assert rel_l2(got0[0], oracle.range_compress(radar, raw[:1].numpy())[0]) <= RC_TOL
+
+
+def test_range_window_bad_arguments():
+    radar = synth.Radar(range_start=5000.0, n_pulses=1, n_range=1024, upsample=1)
+    plan = sar.sar_plan_create(radar, None, 0)
+    L = sar.lib()
+    assert L.sar_plan_set_range_window(plan.handle, 3, 4, 35.0) == 1
+    assert L.sar_plan_set_range_window(plan.handle, sar.SAR_WINDOW_TAYLOR, 1, 35.0) == 1
+    assert L.sar_plan_set_range_window(plan.handle, sar.SAR_WINDOW_TAYLOR, 4, 0.0) == 1
+    assert L.sar_plan_set_range_window(plan.handle, sar.SAR_WINDOW_TAYLOR, 4, float("nan")) == 1
+    assert L.sar_plan_set_range_window(plan.handle, sar.SAR_WINDOW_HAMMING, 0, 0.0) == 0
