@@ -4,10 +4,10 @@ backprojection as hand-written CUDA kernels for sm_103a behind a small C ABI
 function names are the C entry points'."""
 from ._binding import (SAR_OK, SAR_RC_NATURAL, SAR_RC_POLYPHASE, SAR_WINDOW_HAMMING, SAR_WINDOW_NONE, SAR_WINDOW_TAYLOR, Plan, SarError, declared_symbols, lib, library_path, sar_backproject,
                        sar_form_image, sar_form_image_host, sar_plan_create, sar_plan_destroy,
-                       sar_plan_kernel_times, sar_plan_last_launches, sar_plan_set_range_window, sar_plan_set_rc_layout, sar_plan_set_timing, sar_plan_sync, sar_range_compress, sar_status_string,
+                       sar_plan_kernel_times, sar_plan_last_launches, sar_plan_set_pulse_weights, sar_plan_set_range_window, sar_plan_set_rc_layout, sar_plan_set_timing, sar_plan_sync, sar_range_compress, sar_status_string,
                        sar_workspace_size)
 from .build import build as build_library
 
 __all__ = ["SAR_OK", "SAR_RC_NATURAL", "SAR_RC_POLYPHASE", "SAR_WINDOW_HAMMING", "SAR_WINDOW_NONE", "SAR_WINDOW_TAYLOR", "Plan", "SarError", "build_library", "declared_symbols", "lib", "library_path", "sar_backproject",
-           "sar_form_image", "sar_form_image_host", "sar_plan_create", "sar_plan_destroy", "sar_plan_kernel_times", "sar_plan_last_launches", "sar_plan_set_range_window", "sar_plan_set_rc_layout", "sar_plan_set_timing",
+           "sar_form_image", "sar_form_image_host", "sar_plan_create", "sar_plan_destroy", "sar_plan_kernel_times", "sar_plan_last_launches", "sar_plan_set_pulse_weights", "sar_plan_set_range_window", "sar_plan_set_rc_layout", "sar_plan_set_timing",
            "sar_plan_sync", "sar_range_compress", "sar_status_string", "sar_workspace_size"]

@@ -71,6 +71,7 @@ def load_library(path: str):
         "sar_plan_set_rc_layout": ([P, ctypes.c_int], ctypes.c_int),
         "sar_plan_set_timing": ([P, ctypes.c_int], ctypes.c_int),
         "sar_plan_set_range_window": ([P, ctypes.c_int, I32, ctypes.c_double], ctypes.c_int),
+        "sar_plan_set_pulse_weights": ([P, P], ctypes.c_int),
         "sar_plan_kernel_times": ([P, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -277,3 +278,17 @@ def sar_plan_set_range_window(plan: Plan, window: int, taylor_nbar: int = 4, tay
     """Weight the plan's matched filter: SAR_WINDOW_NONE, SAR_WINDOW_HAMMING or SAR_WINDOW_TAYLOR."""
     _check(lib().sar_plan_set_range_window(plan.handle, int(window), int(taylor_nbar), float(taylor_sll_db)),
            "sar_plan_set_range_window")
+
+
+def sar_plan_set_pulse_weights(plan: Plan, weights) -> None:
+    """Per-pulse real weights for later backprojections: a CUDA float32 tensor [Na] (kept referenced by
+    the plan while set), or None for unit weights."""
+    if weights is None:
+        _check(lib().sar_plan_set_pulse_weights(plan.handle, None), "sar_plan_set_pulse_weights")
+        plan.weights = None
+        return
+    if tuple(weights.shape) != (plan.radar.n_pulses,):
+        raise ValueError(f"weights must be [{plan.radar.n_pulses}]")
+    _check(lib().sar_plan_set_pulse_weights(plan.handle, _dev_tensor(weights, torch.float32, "weights", plan.device)),
+           "sar_plan_set_pulse_weights")
+    plan.weights = weights

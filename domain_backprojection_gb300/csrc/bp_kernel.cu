@@ -374,7 +374,8 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
         cp_async_commit();
     };
     // raw samples -> (tau, sigma) entries of the staged windows
-    auto transform = [&](int count, const int4 *win) {
+    // (pulse n + p of the batch weighted by args.weights[n + p] when the plan has pulse weights)
+    auto transform = [&](int n, int count, const int4 *win) {
         for (int p = warp; p < count; p += kWarps) {
             const int4 wv = win[p];
             const int e_lo = wv.y;
@@ -382,11 +383,21 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
             const float2 *rr = raw + p * rw;
             float4 *row = stage + p * stride;
             const float im0 = (float)(e_lo - wh) - 0.5f;
-            for (int c = lane; c < nent; c += 32) {
-                const float2 v0 = rr[c], v1 = rr[c + 1];
-                const float sr = v1.x - v0.x, si = v1.y - v0.y;
-                const float im = im0 + (float)c;
-                row[c] = make_float4(fmaf(-im, sr, v0.x), fmaf(-im, si, v0.y), sr, si);
+            if (args.weights) {
+                const float wgt = __ldg(args.weights + n + p);
+                for (int c = lane; c < nent; c += 32) {
+                    const float2 v0 = rr[c], v1 = rr[c + 1];
+                    const float sr = v1.x - v0.x, si = v1.y - v0.y;
+                    const float im = im0 + (float)c;
+                    row[c] = make_float4(wgt * fmaf(-im, sr, v0.x), wgt * fmaf(-im, si, v0.y), wgt * sr, wgt * si);
+                }
+            } else {
+                for (int c = lane; c < nent; c += 32) {
+                    const float2 v0 = rr[c], v1 = rr[c + 1];
+                    const float sr = v1.x - v0.x, si = v1.y - v0.y;
+                    const float im = im0 + (float)c;
+                    row[c] = make_float4(fmaf(-im, sr, v0.x), fmaf(-im, si, v0.y), sr, si);
+                }
             }
         }
     };
@@ -415,7 +426,7 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
     if (pb > 0) issue_raw(p_begin, pb, wins);
     cp_async_wait_all();
     __syncthreads();
-    if (pb > 0) transform(pb, wins);
+    if (pb > 0) transform(p_begin, pb, wins);
     __syncthreads();
 
     int buf = 0;
@@ -444,7 +455,7 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
         if ((int)threadIdx.x < pb2) put_params(threadIdx.x, nx0, nx1, nx2, quads + 4 * pb_cap * buf2, wins + pb_cap * buf2);
         cp_async_wait_all();
         __syncthreads();
-        if (pb1 > 0) transform(pb1, wins + pb_cap * buf1);
+        if (pb1 > 0) transform(n1, pb1, wins + pb_cap * buf1);
         __syncthreads();
         n0 = n1;
         pb = pb1;

@@ -644,6 +644,15 @@ sar_status sar_plan_sync(sar_plan plan, void *stream)
 
 int32_t sar_plan_last_launches(sar_plan plan) { return plan ? plan->last_launches : 0; }
 
+sar_status sar_plan_set_pulse_weights(sar_plan plan, const float *weights)
+{
+    if (!plan) return SAR_ERR_INVALID_ARG;
+    if (!plan->has_grid) return SAR_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(weights) & 3u) return SAR_ERR_INVALID_ARG;
+    plan->bp.weights = weights;
+    return SAR_OK;
+}
+
 sar_status sar_plan_set_range_window(sar_plan plan, sar_window window, int32_t taylor_nbar, double taylor_sll_db)
 {
     if (!plan) return SAR_ERR_INVALID_ARG;

@@ -81,6 +81,7 @@ struct BpArgs {
     const float2 *rc;        // [Na][U Nr], natural order or polyphase planes (planar != 0)
     int planar, u_shift, u_mask, n_range;   // planes: sample I of a line at (I & u_mask) Nr + (I >> u_shift)
     const double *pos;       // [Na][3]
+    const float *weights;    // [Na] real pulse weights, or null for 1
     float2 *image;           // [ny][nx]
     int pulse_begin, pulse_end;
     int accumulate;

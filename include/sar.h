@@ -191,6 +191,18 @@ typedef enum { SAR_WINDOW_NONE = 0, SAR_WINDOW_HAMMING = 1, SAR_WINDOW_TAYLOR = 
  * (and image formations) use the new one.  SAR_ERR_CUDA if the upload fails. */
 sar_status sar_plan_set_range_window(sar_plan plan, sar_window window, int32_t taylor_nbar, double taylor_sll_db);
 
+/* Azimuth (pulse) weighting of the backprojection: with weights non-NULL, every
+ * later backprojection on this plan sums weights[n] * L_n(...) * exp(...) over
+ * pulses n, i.e. pulse n's compressed line scaled by a real weight (an aperture
+ * taper such as Hamming or Taylor over the pulses lowers the azimuth sidelobes
+ * the way range weighting lowers the range ones).  weights: device [Na] float32,
+ * 4-byte aligned, owned by the caller, read by the kernels and left unchanged;
+ * it must stay valid while backprojections that use it are in flight.  NULL
+ * restores unit weights.  The weights are applied while the compressed samples
+ * are staged, so they cost nothing per pixel.  SAR_ERR_UNSUPPORTED for a plan
+ * without a grid. */
+sar_status sar_plan_set_pulse_weights(sar_plan plan, const float *weights);
+
 /* Kernel timing, for benchmarks (no counterpart in the pages).  With enable != 0,
  * each later range-compression call records a pair of CUDA events on its stream
  * around the transform kernel, and each backprojection around the pixel kernel

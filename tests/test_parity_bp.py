@@ -298,3 +298,30 @@ def test_form_image_with_range_weighting():
     assert rel_l2(img.cpu().numpy(), ref) <= IMG_TOL
     centres = target_pixels(s)
     check_peaks(img.cpu().numpy(), ref, s["grid"], centres, 6)
+
+
+def test_pulse_weights():
+    # a Hamming taper over the aperture: the image is the oracle's backprojection of the compressed
+    # lines each scaled by its weight; unit weights give the unweighted image bit for bit
+    s = _small_case(48, 40, na=96)
+    na = s["radar"].n_pulses
+    plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
+    rc = sar.sar_range_compress(plan, s["raw"])
+    plain = sar.sar_backproject(plan, rc, s["pos"])
+    w = torch.tensor(np.hamming(na), dtype=torch.float32, device="cuda")
+    sar.sar_plan_set_pulse_weights(plan, w)
+    weighted = sar.sar_backproject(plan, rc, s["pos"])
+    part = sar.sar_backproject(plan, rc, s["pos"], 0, 50)
+    sar.sar_backproject(plan, rc, s["pos"], 50, na - 50, image=part, accumulate=True)
+    sar.sar_plan_set_pulse_weights(plan, torch.ones(na, dtype=torch.float32, device="cuda"))
+    ones = sar.sar_backproject(plan, rc, s["pos"])
+    sar.sar_plan_set_pulse_weights(plan, None)
+    again = sar.sar_backproject(plan, rc, s["pos"])
+    sar.sar_plan_sync(plan)
+    rcw = rc.cpu().numpy() * w.cpu().numpy()[:, None]
+    ref = oracle.backproject(s["radar"], s["grid"], rcw, s["pos"].cpu().numpy())
+    assert rel_l2(weighted.cpu().numpy(), ref) <= IMG_TOL
+    assert rel_l2(part.cpu().numpy(), ref) <= IMG_TOL
+    assert torch.equal(ones, plain) and torch.equal(again, plain)
+    with pytest.raises(ValueError):
+        sar.sar_plan_set_pulse_weights(plan, torch.ones(na + 1, dtype=torch.float32, device="cuda"))
