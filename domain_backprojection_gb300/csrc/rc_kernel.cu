@@ -549,26 +549,26 @@ __global__ void __launch_bounds__(200, kRcMixedCtas) rc_mixed6000_kernel(const f
             mixed_dft6000(x, buf, args.tw);
 #pragma unroll
             for (int p = 0; p < E; p++) out[t + T * p] = cconj(x[p]);
-            continue;
-        }
-        float2 y[E];
+        } else {
+            float2 y[E];
 #pragma unroll
-        for (int p = 0; p < E; p++) y[p] = x[p];
-        for (int u = 0; u < U; u++) {
+            for (int p = 0; p < E; p++) y[p] = x[p];
+            for (int u = 0; u < U; u++) {
 #pragma unroll
-            for (int p = 0; p < E; p++) x[p] = cconj(y[p]);
-            mixed_dft6000(x, buf, args.tw);
-            if (args.planar) {
-                float2 *plane = out + (int64_t)u * N;
+                for (int p = 0; p < E; p++) x[p] = cconj(y[p]);
+                mixed_dft6000(x, buf, args.tw);
+                if (args.planar) {
+                    float2 *plane = out + (int64_t)u * N;
 #pragma unroll
-                for (int p = 0; p < E; p++) plane[t + T * p] = cconj(x[p]);
-            } else {
+                    for (int p = 0; p < E; p++) plane[t + T * p] = cconj(x[p]);
+                } else {
 #pragma unroll
-                for (int p = 0; p < E; p++) out[(int64_t)U * (t + T * p) + u] = cconj(x[p]);
-            }
-            if (u + 1 < U) {
+                    for (int p = 0; p < E; p++) out[(int64_t)U * (t + T * p) + u] = cconj(x[p]);
+                }
+                if (u + 1 < U) {
 #pragma unroll
-                for (int p = 0; p < E; p++) y[p] = cmul(y[p], __ldg(args.ramp + t + T * p));
+                    for (int p = 0; p < E; p++) y[p] = cmul(y[p], __ldg(args.ramp + t + T * p));
+                }
             }
         }
     }
