@@ -279,11 +279,25 @@ def rc_kernel_name(nr):
     return "rc_mixed6000_kernel" if nr == 6000 else "rc_fused_kernel"
 
 
-def profile_case():
+def profile_case(case="spotlight"):
     import torch
     import domain_backprojection_gb300 as sar
     import synth
 
+    if case.startswith("sweep"):
+        nr = int(case[len("sweep"):])
+        if nr not in synth.RC_SWEEP_NR:
+            raise SystemExit(f"unknown profile case {case!r}")
+        sc = synth.make_rc_sweep(nr, n_lines=4096, device="cuda")
+        plan = sar.sar_plan_create(sc["radar"], None, 0)
+        out = torch.empty_like(sc["raw"])
+        for _ in range(3):
+            sar.sar_range_compress(plan, sc["raw"], out)
+        sar.sar_plan_sync(plan)
+        print(json.dumps({"profile_case": "ok", "workload": f"range-only sweep, 4096 lines of {nr} samples, U=1"}))
+        return
+    if case != "spotlight":
+        raise SystemExit(f"unknown profile case {case!r}")
     scene = synth.make_scene(CONFIG_ID, device="cuda")
     radar = scene["radar"]
     plan = sar.sar_plan_create(radar, scene["grid"], 0)
@@ -400,13 +414,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rc-sweep", action="store_true")
-    ap.add_argument("--profile-case", action="store_true",
-                    help="form two images of the spotlight scene (RC then BP, polyphase planes) and exit, untimed; "
-                         "the launch sequence profiler captures are taken on")
+    ap.add_argument("--profile-case", nargs="?", const="spotlight", default=None,
+                    help="run a short untimed case for profiler captures and exit: 'spotlight' (default) forms two "
+                         "images of the spotlight scene (RC then BP, polyphase planes); 'sweepNR' (NR in 4096, 8192, "
+                         "6000) range-compresses the 4096 lines of the range-only workload three times")
     args = ap.parse_args()
     rank, world, local_rank = rank_env()
     if args.profile_case:
-        profile_case()
+        profile_case(args.profile_case)
         return
     if world > 1 and args.impl == "ours":
         import torch

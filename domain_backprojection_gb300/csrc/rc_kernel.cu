@@ -309,14 +309,24 @@ __global__ void __launch_bounds__(512) rc_fused_kernel(const float2 *__restrict_
 // when log2 Nr is not a multiple of 4) in the same self-sorting Stockham
 // order as above; the first pass reads the thread's registers, the last pass
 // leaves its results in registers in the same t + T p layout, and the passes
-// in between exchange through one padded shared-memory buffer (one element of
-// padding per 16 keeps the strided reads free of bank conflicts).  So the
+// in between exchange through two padded shared-memory buffers used in turn
+// (one element of padding per 16 keeps the strided reads free of bank
+// conflicts; alternating buffers leaves one barrier per exchange).  So the
 // forward transform's output, the filter multiply and the inverse transforms'
 // inputs never touch shared memory, and each transform costs log16(Nr) - 1
 // exchanges.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ int pad16(int i) { return i + (i >> 4); }
+
+// Twiddle load kept opaque to the compiler: the forward and inverse transforms of a line read the
+// same twiddles, and merging their powers across the two would keep ~60 more registers live.
+__device__ __forceinline__ float2 ld_twiddle(const float2 *p)
+{
+    float2 v;
+    asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
 
 // w^p for p = 0 .. R-1 from w^1, multiplying powers of two (depth log2 R)
 template <int R>
@@ -332,10 +342,11 @@ __device__ __forceinline__ void twiddle_powers(float2 w1, float2 *w)
 }
 
 // One pass of radix R after L elements have been combined (L > 1): every
-// thread loads its 16/R butterflies from the buffer, then (after a barrier)
-// writes them back transformed, or keeps them when kLast.
-template <int N, int R, int L, bool kLast>
-__device__ __forceinline__ void reg_pass(float2 (&x)[16], float2 *buf, const float2 *__restrict__ tw)
+// thread loads its 16/R butterflies from `src`, transforms them and writes them
+// to `dst` followed by a barrier, or keeps them in registers when kLast.  With
+// one buffer (src == dst) a barrier also separates the loads from the stores.
+template <int N, int R, int L, bool kLast, bool kOneBuf>
+__device__ __forceinline__ void reg_pass(float2 (&x)[16], const float2 *src, float2 *dst, const float2 *__restrict__ tw)
 {
     constexpr int T = N / 16, SP = N / (L * R), NB = 16 / R;
     const int t = threadIdx.x;
@@ -344,21 +355,21 @@ __device__ __forceinline__ void reg_pass(float2 (&x)[16], float2 *buf, const flo
         const int b = t + T * i;
         const int jp = b % SP, kp = b / SP;
 #pragma unroll
-        for (int p = 0; p < R; p++) x[i * R + p] = buf[pad16(kp * SP * R + jp + SP * p)];
+        for (int p = 0; p < R; p++) x[i * R + p] = src[pad16(kp * SP * R + jp + SP * p)];
     }
-    __syncthreads();
+    if (kOneBuf && !kLast) __syncthreads();
 #pragma unroll
     for (int i = 0; i < NB; i++) {
         const int b = t + T * i;
         const int jp = b % SP, kp = b / SP;
         float2 w[R];
-        twiddle_powers<R>(__ldg(tw + SP * kp), w);
+        twiddle_powers<R>(ld_twiddle(tw + SP * kp), w);
 #pragma unroll
         for (int p = 1; p < R; p++) x[i * R + p] = cmul(x[i * R + p], w[p]);
         Dft<R>::run(x + i * R);
         if (!kLast) {
 #pragma unroll
-            for (int q = 0; q < R; q++) buf[pad16((kp + L * q) * SP + jp)] = x[i * R + q];
+            for (int q = 0; q < R; q++) dst[pad16((kp + L * q) * SP + jp)] = x[i * R + q];
         }
     }
     if (!kLast) __syncthreads();
@@ -375,68 +386,179 @@ __device__ __forceinline__ void reg_pass(float2 (&x)[16], float2 *buf, const flo
 }
 
 // Forward DFT of the line held as x[p] = element t + T p; result in the same layout.
-template <int N>
-__device__ __forceinline__ void reg_dft(float2 (&x)[16], float2 *buf, const float2 *__restrict__ tw)
+// With two buffers (kTwoBuf) the exchanges alternate between them, so that each needs one
+// barrier: every write goes to the buffer read two exchanges earlier, and the barrier of the
+// exchange in between orders all of those reads before it.  The pair (a, b) carries the
+// alternation from one transform to the next; `a` is the buffer the next exchange writes.  With
+// one buffer (a == b) each exchange takes a second barrier before its stores, and the transform
+// ends with one, so that the next transform may write the buffer.
+template <int N, bool kTwoBuf>
+__device__ __forceinline__ void reg_dft(float2 (&x)[16], float2 *&a, float2 *&b, const float2 *__restrict__ tw)
 {
     constexpr int T = N / 16;
+    constexpr bool k1 = !kTwoBuf;
     const int t = threadIdx.x;
     Dft<16>::run(x);                                            // pass 1: L = 1, no twiddles
 #pragma unroll
-    for (int q = 0; q < 16; q++) buf[pad16(q * T + t)] = x[q];
+    for (int q = 0; q < 16; q++) a[pad16(q * T + t)] = x[q];
     __syncthreads();
     if constexpr (N == 512) {
-        reg_pass<N, 16, 16, false>(x, buf, tw);
-        reg_pass<N, 2, 256, true>(x, buf, tw);
+        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
+        reg_pass<N, 2, 256, true, k1>(x, b, nullptr, tw);
     } else if constexpr (N == 1024) {
-        reg_pass<N, 16, 16, false>(x, buf, tw);
-        reg_pass<N, 4, 256, true>(x, buf, tw);
+        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
+        reg_pass<N, 4, 256, true, k1>(x, b, nullptr, tw);
     } else if constexpr (N == 2048) {
-        reg_pass<N, 16, 16, false>(x, buf, tw);
-        reg_pass<N, 8, 256, true>(x, buf, tw);
+        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
+        reg_pass<N, 8, 256, true, k1>(x, b, nullptr, tw);
     } else if constexpr (N == 4096) {
-        reg_pass<N, 16, 16, false>(x, buf, tw);
-        reg_pass<N, 16, 256, true>(x, buf, tw);
+        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
+        reg_pass<N, 16, 256, true, k1>(x, b, nullptr, tw);
     } else {
         static_assert(N == 8192, "unsupported line length");
-        reg_pass<N, 16, 16, false>(x, buf, tw);
-        reg_pass<N, 16, 256, false>(x, buf, tw);
-        reg_pass<N, 2, 4096, true>(x, buf, tw);
+        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
+        reg_pass<N, 16, 256, false, k1>(x, b, a, tw);
+        reg_pass<N, 2, 4096, true, k1>(x, a, nullptr, tw);
+        float2 *c = a;                                          // three exchanges: the next one writes b
+        a = b;
+        b = c;
     }
-    __syncthreads();                                            // the buffer is free for the next transform
+    if constexpr (!kTwoBuf) __syncthreads();                    // the buffer is free for the next transform
 }
 
-template <int N>
-__global__ void __launch_bounds__(N / 16, N == 4096 ? 2 : 1) rc_reg_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc,
-                                                        int64_t n_lines, RcArgs args)
+// ---------------------------------------------------------------------------
+// Line staging by the tensor memory accelerator: each CTA stays resident and
+// loops over lines; while it transforms one line out of its registers, one
+// bulk copy (cp.async.bulk, completion counted in bytes on an mbarrier)
+// brings the next raw line into a shared-memory stage, so the load latency is
+// hidden even with a single CTA per SM.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void stage_barrier_init(uint64_t *bar)
 {
-    extern __shared__ float4 smem4[];
-    float2 *buf = reinterpret_cast<float2 *>(smem4);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// One bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) into the stage,
+// announced on the barrier as its expected transaction count.  Issued by one thread, after a
+// CTA barrier that ended every generic-proxy read of the stage.
+__device__ __forceinline__ void stage_line(uint64_t *bar, void *stage, const void *src, uint32_t bytes)
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(stage)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool stage_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the barrier phase of the given parity; false if kWaitLimitNs (or an iteration cap)
+// passed first.
+__device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity)
+{
+    if (stage_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 30); i++) {
+        if (stage_try_wait(bar, parity)) return true;
+        if ((i & 63) == 63 && global_ns() - t0 > kWaitLimitNs) break;
+    }
+    return false;
+}
+
+// Resident CTAs per SM each line kernel is built for: the register budget that __launch_bounds__
+// enforces.  16 warps per SM for short lines; 3 CTAs for 4096-point lines without upsampling (no
+// copy of the spectrum to keep), 2 with it; one 16-warp CTA for 8192-point lines.
+template <int N, bool kMulti>
+__host__ __device__ constexpr int rc_reg_min_ctas()
+{
+    return N == 8192 ? 1 : N == 4096 ? (kMulti ? 2 : 3) : (16 * 32) / (N / 16);
+}
+
+// Whether the (N, U) line kernel stages lines by bulk copy (persistent CTAs) or loads them
+// straight into registers (one CTA per line).  Staging pays where a single CTA holds the SM
+// (8192-point lines), so nothing else covers the load latency.  Where two or three CTAs share an
+// SM, their loads overlap each other's transforms, and the stage's shared memory would instead
+// take L1 capacity from the filter and ramp tables (measured on GB300: 4096-point lines without
+// upsampling 0.081 ms unstaged against 0.085 ms staged, with upsampling 0.381 against 0.405 ms).
+template <int N, bool kMulti>
+__host__ __device__ constexpr bool rc_reg_staged() { return N == 8192; }
+
+// Whether the (N, U) line kernel alternates two exchange buffers (one barrier per exchange) or
+// uses one (two barriers per exchange, half the shared memory).  One buffer where three CTAs share
+// an SM: their six buffers would leave L1 too little room for the filter table (measured on
+// GB300: 4096-point lines without upsampling 0.081 ms with one buffer, 0.089 ms with two).
+template <int N, bool kMulti>
+__host__ __device__ constexpr bool rc_reg_two_buffers() { return rc_reg_min_ctas<N, kMulti>() < 3; }
+
+// Exchange buffers of N + N/16 entries, then (staged kernels) the raw-line stage and its barrier.
+template <int N, bool kMulti>
+constexpr size_t rc_reg_smem()
+{
+    return (rc_reg_two_buffers<N, kMulti>() ? 2 : 1) * (size_t)(N + N / 16) * sizeof(float2) +
+           (rc_reg_staged<N, kMulti>() ? (size_t)N * sizeof(float2) + 16 : 0);
+}
+
+// One line held in registers (x[p] = raw element t + T p): forward transform, matched filter,
+// U inverse transforms, stores of the compressed line.
+template <int N, bool kMulti>
+__device__ __forceinline__ void rc_reg_line(float2 (&x)[16], float2 *&a, float2 *&b, float2 *__restrict__ out,
+                                            const RcArgs &args)
+{
     constexpr int T = N / 16;
     const int t = threadIdx.x;
-    const int U = args.u;
-    for (int64_t line = blockIdx.x; line < n_lines; line += gridDim.x) {
-        float2 x[16], y[16];
-        const float2 *src = raw + line * N;
+    if constexpr (!kMulti) {
+        // forward transform, filter and conjugate, inverse transform: one copy of the transform
+        // code in a two-trip loop (two inlined copies spill)
+#pragma unroll 1
+        for (int k = 0; k < 2; k++) {
+            reg_dft<N, rc_reg_two_buffers<N, kMulti>()>(x, a, b, args.tw);
+            if (k == 0) {
 #pragma unroll
-        for (int p = 0; p < 16; p++) x[p] = __ldg(src + t + T * p);
-        reg_dft<N>(x, buf, args.tw);
-        // matched filter
+                for (int p = 0; p < 16; p++) x[p] = cconj(cmul(x[p], __ldg(args.h + t + T * p)));
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < 16; p++) out[t + T * p] = cconj(x[p]);
+    } else {
+        const int U = args.u;
+        reg_dft<N, rc_reg_two_buffers<N, kMulti>()>(x, a, b, args.tw);
+        // matched filter (with the IDFT's 1 / Nr)
+        float2 y[16];
 #pragma unroll
         for (int p = 0; p < 16; p++) y[p] = cmul(x[p], __ldg(args.h + t + T * p));
-        float2 *out = rc + line * (int64_t)(U * N);
         for (int u = 0; u < U; u++) {
             // y = Y exp(+j 2 pi k_s u / (U N)); inverse transform by the conjugate identity
 #pragma unroll
             for (int p = 0; p < 16; p++) x[p] = cconj(y[p]);
-            reg_dft<N>(x, buf, args.tw);
-            if (args.planar || U == 1) {
+            reg_dft<N, rc_reg_two_buffers<N, kMulti>()>(x, a, b, args.tw);
+            if (args.planar) {
                 float2 *plane = out + (int64_t)u * N;
 #pragma unroll
                 for (int p = 0; p < 16; p++) plane[t + T * p] = cconj(x[p]);
             } else {
 #pragma unroll
-                for (int p = 0; p < 16; p++)
-                    out[(int64_t)U * (t + T * p) + u] = cconj(x[p]);
+                for (int p = 0; p < 16; p++) out[(int64_t)U * (t + T * p) + u] = cconj(x[p]);
             }
             if (u + 1 < U) {
 #pragma unroll
@@ -446,8 +568,50 @@ __global__ void __launch_bounds__(N / 16, N == 4096 ? 2 : 1) rc_reg_kernel(const
     }
 }
 
-template <int N>
-size_t rc_reg_smem() { return (size_t)(N + N / 16) * sizeof(float2); }
+template <int N, bool kMulti>
+__global__ void __launch_bounds__(N / 16, (rc_reg_min_ctas<N, kMulti>()))
+    rc_reg_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc, int64_t n_lines, RcArgs args)
+{
+    extern __shared__ float4 smem4[];
+    constexpr int T = N / 16;
+    float2 *a = reinterpret_cast<float2 *>(smem4);             // exchange buffers, N + N/16 entries each
+    float2 *b = rc_reg_two_buffers<N, kMulti>() ? a + N + N / 16 : a;
+    const int t = threadIdx.x;
+    const int64_t line_elems = (int64_t)(kMulti ? args.u : 1) * N;
+    int64_t line = blockIdx.x;
+    if constexpr (!rc_reg_staged<N, kMulti>()) {
+        for (; line < n_lines; line += gridDim.x) {
+            float2 x[16];
+            const float2 *src = raw + line * N;
+#pragma unroll
+            for (int p = 0; p < 16; p++) x[p] = __ldg(src + t + T * p);
+            rc_reg_line<N, kMulti>(x, a, b, rc + line * line_elems, args);
+        }
+    } else {
+        float2 *stage = (rc_reg_two_buffers<N, kMulti>() ? b : a) + N + N / 16;   // raw line, N entries
+                                                                // (16-byte aligned)
+        uint64_t *bar = reinterpret_cast<uint64_t *>(stage + N);
+        if (line >= n_lines) return;
+        if (t == 0) stage_barrier_init(bar);
+        __syncthreads();
+        if (t == 0) stage_line(bar, stage, raw + line * N, N * sizeof(float2));
+        uint32_t parity = 0;
+        for (; line < n_lines; line += gridDim.x) {
+            const bool ok = stage_wait(bar, parity);
+            parity ^= 1u;
+            float2 x[16];
+#pragma unroll
+            for (int p = 0; p < 16; p++) x[p] = stage[t + T * p];
+            if (__syncthreads_or(!ok)) {                        // the stage is free again (or the copy never came)
+                if (t == 0) atomicOr(args.err, kDevErrTimeout);
+                return;
+            }
+            if (t == 0 && line + gridDim.x < n_lines)
+                stage_line(bar, stage, raw + (line + gridDim.x) * N, N * sizeof(float2));
+            rc_reg_line<N, kMulti>(x, a, b, rc + line * line_elems, args);
+        }
+    }
+}
 
 // ---------------------------------------------------------------------------
 // Register-resident transform for Nr = 6000 = 2^4 3 5^3 (the non-power-of-two
@@ -457,8 +621,8 @@ size_t rc_reg_smem() { return (size_t)(N + N / 16) * sizeof(float2); }
 // the first pass reads registers, the last leaves its output in registers in
 // the t + T p layout, and the passes in between exchange through shared memory.
 // ---------------------------------------------------------------------------
-template <int N, int E, int R, int L, bool kFirst, bool kLast>
-__device__ __forceinline__ void mixed_pass(float2 (&x)[E], float2 *buf, const float2 *__restrict__ tw)
+template <int N, int E, int R, int L, bool kFirst, bool kLast, bool kOneBuf>
+__device__ __forceinline__ void mixed_pass(float2 (&x)[E], const float2 *src, float2 *dst, const float2 *__restrict__ tw)
 {
     constexpr int T = N / E, SP = N / (L * R), NB = E / R;
     static_assert(E % R == 0 && N % (L * R) == 0, "pass does not fit the layout");
@@ -478,9 +642,9 @@ __device__ __forceinline__ void mixed_pass(float2 (&x)[E], float2 *buf, const fl
             const int b = t + T * i;
             const int jp = b % SP, kp = b / SP;
 #pragma unroll
-            for (int p = 0; p < R; p++) x[i * R + p] = buf[kp * SP * R + jp + SP * p];
+            for (int p = 0; p < R; p++) x[i * R + p] = src[kp * SP * R + jp + SP * p];
         }
-        __syncthreads();
+        if (kOneBuf && !kLast) __syncthreads();
     }
 #pragma unroll
     for (int i = 0; i < NB; i++) {
@@ -488,14 +652,14 @@ __device__ __forceinline__ void mixed_pass(float2 (&x)[E], float2 *buf, const fl
         const int jp = b % SP, kp = b / SP;
         if (!kFirst) {
             float2 w[R];
-            twiddle_powers<R>(__ldg(tw + SP * kp), w);
+            twiddle_powers<R>(ld_twiddle(tw + SP * kp), w);
 #pragma unroll
             for (int p = 1; p < R; p++) x[i * R + p] = cmul(x[i * R + p], w[p]);
         }
         Dft<R>::run(x + i * R);
         if (!kLast) {
 #pragma unroll
-            for (int q = 0; q < R; q++) buf[(kp + L * q) * SP + jp] = x[i * R + q];
+            for (int q = 0; q < R; q++) dst[(kp + L * q) * SP + jp] = x[i * R + q];
         }
     }
     if (!kLast) __syncthreads();
@@ -512,64 +676,127 @@ __device__ __forceinline__ void mixed_pass(float2 (&x)[E], float2 *buf, const fl
 }
 
 // Forward DFT of the 6000-point line held as x[p] = element t + T p; result in the same layout.
-__device__ __forceinline__ void mixed_dft6000(float2 (&x)[30], float2 *buf, const float2 *__restrict__ tw)
+// Exchanges use one or two buffers as in reg_dft; with two, there are three exchanges, so the
+// next transform starts on the other buffer.
+template <bool kTwoBuf>
+__device__ __forceinline__ void mixed_dft6000(float2 (&x)[30], float2 *&a, float2 *&b, const float2 *__restrict__ tw)
 {
-    mixed_pass<6000, 30, 10, 1, true, false>(x, buf, tw);
-    mixed_pass<6000, 30, 10, 10, false, false>(x, buf, tw);
-    mixed_pass<6000, 30, 10, 100, false, false>(x, buf, tw);
-    mixed_pass<6000, 30, 6, 1000, false, true>(x, buf, tw);
-    __syncthreads();                                            // the buffer is free for the next transform
+    constexpr bool k1 = !kTwoBuf;
+    mixed_pass<6000, 30, 10, 1, true, false, k1>(x, nullptr, a, tw);
+    mixed_pass<6000, 30, 10, 10, false, false, k1>(x, a, b, tw);
+    mixed_pass<6000, 30, 10, 100, false, false, k1>(x, b, a, tw);
+    mixed_pass<6000, 30, 6, 1000, false, true, k1>(x, a, nullptr, tw);
+    float2 *c = a;
+    a = b;
+    b = c;
+    if constexpr (!kTwoBuf) __syncthreads();                    // the buffer is free for the next transform
 }
 
-constexpr int kRcMixedCtas = 1;     // the 30-element layout wants ~250 registers; bounding them to fit
-                                    // 2 CTAs per SM spills and runs slower at U = 8
+constexpr int kRcMixedCtas = 1;     // with upsampling the 30-element layout and the spectrum copy want
+                                    // ~250 registers; bounding them to fit 2 CTAs per SM spills.  Without
+                                    // upsampling (no copy) 128 registers suffice and 2 CTAs fit.
+
+// Whether the 6000-point kernel stages lines by bulk copy (persistent CTAs, one per SM: the stage
+// does not fit beside two CTAs' exchange buffers) or loads them into registers (two CTAs per SM
+// without upsampling).
+__host__ __device__ constexpr bool rc_mixed_staged(bool multi) { return multi; }
+
+// Two exchange buffers (one barrier per exchange), or one where two CTAs share an SM and two
+// buffers each would leave L1 too little room for the 48 KB filter table.
+__host__ __device__ constexpr bool rc_mixed_two_buffers(bool multi) { return multi; }
+
+// Exchange buffers of 6000 entries, then (staged) the raw-line stage and its barrier.
+__host__ __device__ constexpr size_t rc_mixed_smem(bool multi)
+{
+    return (rc_mixed_two_buffers(multi) ? 2 : 1) * 6000 * sizeof(float2) +
+           (rc_mixed_staged(multi) ? 6000 * sizeof(float2) + 16 : 0);
+}
 
 template <bool kMulti>
-__global__ void __launch_bounds__(200, kRcMixedCtas) rc_mixed6000_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc,
+__device__ __forceinline__ void rc_mixed_line(float2 (&x)[30], float2 *&a, float2 *&b, float2 *__restrict__ out,
+                                              const RcArgs &args)
+{
+    constexpr int N = 6000, E = 30, T = N / E;
+    const int t = threadIdx.x;
+    if constexpr (!kMulti) {
+        // forward transform, filter (with the IDFT's 1 / Nr) and conjugate, inverse transform
+#pragma unroll 1
+        for (int k = 0; k < 2; k++) {
+            mixed_dft6000<rc_mixed_two_buffers(kMulti)>(x, a, b, args.tw);
+            if (k == 0) {
+#pragma unroll
+                for (int p = 0; p < E; p++) x[p] = cconj(cmul(x[p], __ldg(args.h + t + T * p)));
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < E; p++) out[t + T * p] = cconj(x[p]);
+    } else {
+        const int U = args.u;
+        mixed_dft6000<rc_mixed_two_buffers(kMulti)>(x, a, b, args.tw);
+        // matched filter (with the IDFT's 1 / Nr)
+        float2 y[E];
+#pragma unroll
+        for (int p = 0; p < E; p++) y[p] = cmul(x[p], __ldg(args.h + t + T * p));
+        for (int u = 0; u < U; u++) {
+#pragma unroll
+            for (int p = 0; p < E; p++) x[p] = cconj(y[p]);
+            mixed_dft6000<rc_mixed_two_buffers(kMulti)>(x, a, b, args.tw);
+            if (args.planar) {
+                float2 *plane = out + (int64_t)u * N;
+#pragma unroll
+                for (int p = 0; p < E; p++) plane[t + T * p] = cconj(x[p]);
+            } else {
+#pragma unroll
+                for (int p = 0; p < E; p++) out[(int64_t)U * (t + T * p) + u] = cconj(x[p]);
+            }
+            if (u + 1 < U) {
+#pragma unroll
+                for (int p = 0; p < E; p++) y[p] = cmul(y[p], __ldg(args.ramp + t + T * p));
+            }
+        }
+    }
+}
+
+template <bool kMulti>
+__global__ void __launch_bounds__(200, kMulti ? kRcMixedCtas : 2) rc_mixed6000_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc,
                                                            int64_t n_lines, RcArgs args)
 {
     constexpr int N = 6000, E = 30, T = N / E;
     extern __shared__ float4 smem4[];
-    float2 *buf = reinterpret_cast<float2 *>(smem4);
+    float2 *a = reinterpret_cast<float2 *>(smem4);
+    float2 *b = rc_mixed_two_buffers(kMulti) ? a + N : a;
     const int t = threadIdx.x;
-    const int U = kMulti ? args.u : 1;
-    for (int64_t line = blockIdx.x; line < n_lines; line += gridDim.x) {
-        float2 x[E];
-        const float2 *src = raw + line * N;
+    const int64_t line_elems = (int64_t)(kMulti ? args.u : 1) * N;
+    int64_t line = blockIdx.x;
+    if constexpr (!rc_mixed_staged(kMulti)) {
+        for (; line < n_lines; line += gridDim.x) {
+            float2 x[E];
+            const float2 *src = raw + line * N;
 #pragma unroll
-        for (int p = 0; p < E; p++) x[p] = __ldg(src + t + T * p);
-        mixed_dft6000(x, buf, args.tw);
-        // matched filter (with the IDFT's 1 / Nr)
+            for (int p = 0; p < E; p++) x[p] = __ldg(src + t + T * p);
+            rc_mixed_line<kMulti>(x, a, b, rc + line * line_elems, args);
+        }
+    } else {
+        float2 *stage = (rc_mixed_two_buffers(kMulti) ? b : a) + N;   // 48000 or 96000 bytes in: 16-byte aligned
+        uint64_t *bar = reinterpret_cast<uint64_t *>(stage + N);
+        if (line >= n_lines) return;
+        if (t == 0) stage_barrier_init(bar);
+        __syncthreads();
+        if (t == 0) stage_line(bar, stage, raw + line * N, N * sizeof(float2));
+        uint32_t parity = 0;
+        for (; line < n_lines; line += gridDim.x) {
+            const bool ok = stage_wait(bar, parity);
+            parity ^= 1u;
+            float2 x[E];
 #pragma unroll
-        for (int p = 0; p < E; p++) x[p] = cmul(x[p], __ldg(args.h + t + T * p));
-        float2 *out = rc + line * (int64_t)(U * N);
-        if constexpr (!kMulti) {
-#pragma unroll
-            for (int p = 0; p < E; p++) x[p] = cconj(x[p]);
-            mixed_dft6000(x, buf, args.tw);
-#pragma unroll
-            for (int p = 0; p < E; p++) out[t + T * p] = cconj(x[p]);
-        } else {
-            float2 y[E];
-#pragma unroll
-            for (int p = 0; p < E; p++) y[p] = x[p];
-            for (int u = 0; u < U; u++) {
-#pragma unroll
-                for (int p = 0; p < E; p++) x[p] = cconj(y[p]);
-                mixed_dft6000(x, buf, args.tw);
-                if (args.planar) {
-                    float2 *plane = out + (int64_t)u * N;
-#pragma unroll
-                    for (int p = 0; p < E; p++) plane[t + T * p] = cconj(x[p]);
-                } else {
-#pragma unroll
-                    for (int p = 0; p < E; p++) out[(int64_t)U * (t + T * p) + u] = cconj(x[p]);
-                }
-                if (u + 1 < U) {
-#pragma unroll
-                    for (int p = 0; p < E; p++) y[p] = cmul(y[p], __ldg(args.ramp + t + T * p));
-                }
+            for (int p = 0; p < E; p++) x[p] = stage[t + T * p];
+            if (__syncthreads_or(!ok)) {
+                if (t == 0) atomicOr(args.err, kDevErrTimeout);
+                return;
             }
+            if (t == 0 && line + gridDim.x < n_lines)
+                stage_line(bar, stage, raw + (line + gridDim.x) * N, N * sizeof(float2));
+            rc_mixed_line<kMulti>(x, a, b, rc + line * line_elems, args);
         }
     }
 }
@@ -580,33 +807,100 @@ int rc_block_threads(int n) { return n >= 4096 ? 512 : 256; }
 
 size_t rc_smem_bytes(int n, int u) { return (size_t)(u == 1 ? 2 : 3) * n * sizeof(float2); }
 
+namespace {
+
+template <typename K>
+int resident(K kernel, int threads, size_t smem, int dev)
+{
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return per_sm * sms;
+}
+
+template <int N, bool kMulti>
+cudaError_t set_reg_smem()
+{
+    return cudaFuncSetAttribute(rc_reg_kernel<N, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)rc_reg_smem<N, kMulti>());
+}
+
+// Resident CTAs of a staged (persistent) line kernel; unstaged ones take one CTA per line.
+template <int N, bool kMulti>
+int reg_resident(int dev)
+{
+    if (!rc_reg_staged<N, kMulti>()) return 1 << 20;
+    return resident(rc_reg_kernel<N, kMulti>, N / 16, rc_reg_smem<N, kMulti>(), dev);
+}
+
+
+}  // namespace
+
 cudaError_t rc_configure(int)
 {
-    // the largest supported line (8192 samples) sets the limit, so plans of any size can coexist
+    // every kernel gets its largest shared-memory size, so plans of any size can coexist
     cudaError_t e = cudaFuncSetAttribute(rc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)rc_smem_bytes(8192, 2));
+    if (e == cudaSuccess) e = set_reg_smem<512, false>();
+    if (e == cudaSuccess) e = set_reg_smem<512, true>();
+    if (e == cudaSuccess) e = set_reg_smem<1024, false>();
+    if (e == cudaSuccess) e = set_reg_smem<1024, true>();
+    if (e == cudaSuccess) e = set_reg_smem<2048, false>();
+    if (e == cudaSuccess) e = set_reg_smem<2048, true>();
+    if (e == cudaSuccess) e = set_reg_smem<4096, false>();
+    if (e == cudaSuccess) e = set_reg_smem<4096, true>();
+    if (e == cudaSuccess) e = set_reg_smem<8192, false>();
+    if (e == cudaSuccess) e = set_reg_smem<8192, true>();
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(rc_reg_kernel<8192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)rc_reg_smem<8192>());
+        e = cudaFuncSetAttribute(rc_mixed6000_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rc_mixed_smem(false));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_mixed6000_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rc_mixed_smem(true));
     return e;
 }
 
 bool rc_has_reg_path(int n) { return n == 512 || n == 1024 || n == 2048 || n == 4096 || n == 8192; }
 
+int rc_resident_ctas(int n, int u, int dev)
+{
+    const bool multi = u > 1;
+    switch (n) {
+    case 512: return multi ? reg_resident<512, true>(dev) : reg_resident<512, false>(dev);
+    case 1024: return multi ? reg_resident<1024, true>(dev) : reg_resident<1024, false>(dev);
+    case 2048: return multi ? reg_resident<2048, true>(dev) : reg_resident<2048, false>(dev);
+    case 4096: return multi ? reg_resident<4096, true>(dev) : reg_resident<4096, false>(dev);
+    case 8192: return multi ? reg_resident<8192, true>(dev) : reg_resident<8192, false>(dev);
+    case 6000:
+        if (!rc_mixed_staged(multi)) return 1 << 20;
+        return multi ? resident(rc_mixed6000_kernel<true>, 200, rc_mixed_smem(true), dev)
+                     : resident(rc_mixed6000_kernel<false>, 200, rc_mixed_smem(false), dev);
+    default: return 1 << 20;     // the shared-memory kernel takes one CTA per line (grid-stride beyond 2^20)
+    }
+}
+
+template <int N>
+static void launch_reg(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, unsigned grid, cudaStream_t s)
+{
+    if (a.u > 1) rc_reg_kernel<N, true><<<grid, N / 16, rc_reg_smem<N, true>(), s>>>(raw, rc, n_lines, a);
+    else rc_reg_kernel<N, false><<<grid, N / 16, rc_reg_smem<N, false>(), s>>>(raw, rc, n_lines, a);
+}
+
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s)
 {
     if (n_lines <= 0) return cudaSuccess;
-    const int64_t max_grid = 1 << 20;
-    const unsigned grid = (unsigned)(n_lines < max_grid ? n_lines : max_grid);
+    // staged line kernels are persistent: at most the resident CTAs, each looping over lines
+    const int64_t cap = a.max_ctas > 0 ? a.max_ctas : 1;
+    const unsigned grid = (unsigned)(n_lines < cap ? n_lines : cap);
     switch (a.n) {
-    case 512: rc_reg_kernel<512><<<grid, 512 / 16, rc_reg_smem<512>(), s>>>(raw, rc, n_lines, a); break;
-    case 1024: rc_reg_kernel<1024><<<grid, 1024 / 16, rc_reg_smem<1024>(), s>>>(raw, rc, n_lines, a); break;
-    case 2048: rc_reg_kernel<2048><<<grid, 2048 / 16, rc_reg_smem<2048>(), s>>>(raw, rc, n_lines, a); break;
-    case 4096: rc_reg_kernel<4096><<<grid, 4096 / 16, rc_reg_smem<4096>(), s>>>(raw, rc, n_lines, a); break;
-    case 8192: rc_reg_kernel<8192><<<grid, 8192 / 16, rc_reg_smem<8192>(), s>>>(raw, rc, n_lines, a); break;
+    case 512: launch_reg<512>(a, raw, rc, n_lines, grid, s); break;
+    case 1024: launch_reg<1024>(a, raw, rc, n_lines, grid, s); break;
+    case 2048: launch_reg<2048>(a, raw, rc, n_lines, grid, s); break;
+    case 4096: launch_reg<4096>(a, raw, rc, n_lines, grid, s); break;
+    case 8192: launch_reg<8192>(a, raw, rc, n_lines, grid, s); break;
     case 6000:
-        if (a.u == 1) rc_mixed6000_kernel<false><<<grid, 200, 6000 * sizeof(float2), s>>>(raw, rc, n_lines, a);
-        else rc_mixed6000_kernel<true><<<grid, 200, 6000 * sizeof(float2), s>>>(raw, rc, n_lines, a);
+        if (a.u == 1) rc_mixed6000_kernel<false><<<grid, 200, rc_mixed_smem(false), s>>>(raw, rc, n_lines, a);
+        else rc_mixed6000_kernel<true><<<grid, 200, rc_mixed_smem(true), s>>>(raw, rc, n_lines, a);
         break;
     default: rc_fused_kernel<<<grid, rc_block_threads(a.n), rc_smem_bytes(a.n, a.u), s>>>(raw, rc, n_lines, a); break;
     }

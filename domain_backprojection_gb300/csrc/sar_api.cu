@@ -227,7 +227,11 @@ sar_status setup_rc(sar_plan p)
     a.ptw_lo = p->d_tables + 2 * n + n_hi;
     a.ramp = p->d_tables + 2 * n + n_hi + n_lo;
     a.planar = 0;
-    return cuda_status(sar::rc_configure(n));
+    a.err = p->d_err;
+    e = sar::rc_configure(n);
+    if (e != cudaSuccess) return cuda_status(e);
+    a.max_ctas = sar::rc_resident_ctas(n, U, p->device);
+    return a.max_ctas > 0 ? SAR_OK : SAR_ERR_CUDA;
 }
 
 // Pulse slices for a backprojection of `pulses` pulses: the tiles x slices work units should fill
@@ -638,6 +642,7 @@ sar_status sar_plan_sync(sar_plan plan, void *stream)
         if (e != cudaSuccess) return SAR_ERR_CUDA;
     }
     if (flags & sar::kDevErrBounds) return SAR_ERR_INTERNAL;
+    if (flags & sar::kDevErrTimeout) return SAR_ERR_TIMEOUT;
     if (flags & sar::kDevErrGeometry) return SAR_ERR_UNSUPPORTED;
     return SAR_OK;
 }

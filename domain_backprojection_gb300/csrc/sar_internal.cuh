@@ -16,7 +16,12 @@ constexpr int kMaxPasses = 16;
 enum : int {
     kDevErrBounds = 1,       // a staged-window index fell outside the window (bounds-checked build)
     kDevErrGeometry = 2,     // a tile came too close to the antenna for the range expansion
+    kDevErrTimeout = 4,      // a bounded wait for an asynchronous copy ran out
 };
+
+// Longest a kernel waits for one of its own asynchronous copies before it gives up, sets
+// kDevErrTimeout and returns (nanoseconds of the GPU's global timer).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // ----------------------------------------------------------- range compression
 struct RcArgs {
@@ -32,12 +37,16 @@ struct RcArgs {
     const float2 *ptw_lo;    // exp(-2 pi i lo / (U Nr)), lo < 2^bits
     const float2 *ramp;      // exp(+2 pi i k_s / (U Nr)) for k in [0, Nr), k_s the signed frequency
     int planar;              // output layout: 0 natural (sample U m + u at U m + u), 1 planes (at u Nr + m)
+    int max_ctas;            // CTAs of the line kernel resident on the whole device (its grid cap)
+    int *err;                // device error word
 };
 
 int rc_block_threads(int n);
 bool rc_has_reg_path(int n);
 size_t rc_smem_bytes(int n, int u);
 cudaError_t rc_configure(int n);
+// CTAs of the line kernel for (n, u) that fit on device `dev` at once (0 on error).
+int rc_resident_ctas(int n, int u, int dev);
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s);
 
 // ----------------------------------------------------------- backprojection

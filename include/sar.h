@@ -162,8 +162,10 @@ sar_status sar_plan_set_rc_layout(sar_plan plan, sar_rc_layout layout);
 sar_status sar_form_image_noalloc(sar_plan plan, const void *raw, const double *pos, void *image, void *stream);
 
 /* Synchronise `stream`, then read and clear the plan's device error flags:
- * SAR_ERR_INTERNAL if a bounds check fired, SAR_ERR_UNSUPPORTED if a geometry
- * validity check failed, SAR_ERR_CUDA on an asynchronous CUDA error. */
+ * SAR_ERR_INTERNAL if a bounds check fired, SAR_ERR_TIMEOUT if a kernel gave
+ * up waiting (about 1 s) for one of its own asynchronous line copies and
+ * returned early (its output is then incomplete), SAR_ERR_UNSUPPORTED if a
+ * geometry validity check failed, SAR_ERR_CUDA on an asynchronous CUDA error. */
 sar_status sar_plan_sync(sar_plan plan, void *stream);
 
 /* Static, NUL-terminated description of a status code. */
