@@ -328,6 +328,15 @@ __device__ __forceinline__ float2 ld_twiddle(const float2 *p)
     return v;
 }
 
+// Raw-line load that leaves L1 to the filter, ramp and twiddle tables: each raw sample is read
+// once, and letting the line stream through L1 evicts the tables that every line re-reads.
+__device__ __forceinline__ float2 ld_raw(const float2 *p)
+{
+    float2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+
 // w^p for p = 0 .. R-1 from w^1, multiplying powers of two (depth log2 R)
 template <int R>
 __device__ __forceinline__ void twiddle_powers(float2 w1, float2 *w)
@@ -584,7 +593,7 @@ __global__ void __launch_bounds__(N / 16, (rc_reg_min_ctas<N, kMulti>()))
             float2 x[16];
             const float2 *src = raw + line * N;
 #pragma unroll
-            for (int p = 0; p < 16; p++) x[p] = __ldg(src + t + T * p);
+            for (int p = 0; p < 16; p++) x[p] = ld_raw(src + t + T * p);
             rc_reg_line<N, kMulti>(x, a, b, rc + line * line_elems, args);
         }
     } else {
@@ -773,7 +782,7 @@ __global__ void __launch_bounds__(200, kMulti ? kRcMixedCtas : 2) rc_mixed6000_k
             float2 x[E];
             const float2 *src = raw + line * N;
 #pragma unroll
-            for (int p = 0; p < E; p++) x[p] = __ldg(src + t + T * p);
+            for (int p = 0; p < E; p++) x[p] = ld_raw(src + t + T * p);
             rc_mixed_line<kMulti>(x, a, b, rc + line * line_elems, args);
         }
     } else {
