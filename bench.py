@@ -263,6 +263,8 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": img_h.numel() * 8, "api": "sar_form_image_host"},
         "gpu_launches": launches,
     }
+    if not args.no_bp_variants:
+        out["bp_variants"] = bp_variants(scene, dev, reps=max(5, min(args.steps, 20)))
     if not args.no_rc_sweep:
         out["rc_sweep"] = rc_sweep(dev, peaks, reps=max(10, min(args.steps, 50)))
     if not args.no_cpu_baseline:
@@ -308,6 +310,53 @@ def profile_case(case="spotlight"):
         sar.sar_backproject(plan, rc, scene["pos"])
     sar.sar_plan_sync(plan)
     print(json.dumps({"profile_case": "ok", "workload": "spotlight 4096x4096 U=8, 1024x1024 image"}))
+
+
+def bp_variants(scene, dev, reps=10):
+    """The backprojection variants on the same spotlight scene (polyphase-plane lines, same step as the
+    headline): pixel-kernel time and rate for compensated sums, float16 staging and 8-tap sinc
+    interpolation; and the step (range compression + backprojection) with x2 instead of x8 upsampled
+    lines and sinc interpolation."""
+    import dataclasses
+    import torch
+    import domain_backprojection_gb300 as sar
+
+    radar, grid = scene["radar"], scene["grid"]
+    pp = radar.n_pulses * grid.nx * grid.ny
+    setters = {
+        "compensated": lambda p: sar.sar_plan_set_accumulation(p, sar.SAR_ACCUM_COMPENSATED),
+        "fp16_stage": lambda p: sar.sar_plan_set_stage_precision(p, sar.SAR_STAGE_FP16),
+        "sinc8": lambda p: sar.sar_plan_set_interpolation(p, sar.SAR_INTERP_SINC8),
+        "sinc8_u2": lambda p: sar.sar_plan_set_interpolation(p, sar.SAR_INTERP_SINC8),
+    }
+    res = {}
+    for name, setter in setters.items():
+        r = dataclasses.replace(radar, upsample=2) if name.endswith("_u2") else radar
+        plan = sar.sar_plan_create(r, grid, dev.index)
+        sar.sar_plan_set_rc_layout(plan, sar.SAR_RC_POLYPHASE)
+        setter(plan)
+        rc = sar.sar_range_compress(plan, scene["raw"])
+        img = sar.sar_backproject(plan, rc, scene["pos"])
+        sar.sar_plan_sync(plan)
+        sar.sar_plan_set_timing(plan, True)
+        sar.sar_plan_kernel_times(plan)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            sar.sar_range_compress(plan, scene["raw"], rc)
+            sar.sar_backproject(plan, rc, scene["pos"], image=img)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        sar.sar_plan_sync(plan)
+        kt = sar.sar_plan_kernel_times(plan)
+        bp_ms = kt["bp_ms"] / kt["bp_calls"]
+        step_ms = e0.elapsed_time(e1) / reps
+        res[name] = {"upsample": r.upsample, "bp_kernel_ms": round(bp_ms, 4),
+                     "bp_gpix_pulse_per_s": round(pp / (bp_ms * 1e-3) / 1e9, 1),
+                     "rc_kernel_ms": round(kt["rc_ms"] / kt["rc_calls"], 4), "step_ms": round(step_ms, 4),
+                     "step_gpix_pulse_per_s": round(pp / (step_ms * 1e-3) / 1e9, 1)}
+        del plan, rc, img
+    return res
 
 
 def rc_sweep(dev, peaks, reps=20, n_sets=4):
@@ -414,6 +463,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rc-sweep", action="store_true")
+    ap.add_argument("--no-bp-variants", action="store_true")
     ap.add_argument("--profile-case", nargs="?", const="spotlight", default=None,
                     help="run a short untimed case for profiler captures and exit: 'spotlight' (default) forms two "
                          "images of the spotlight scene (RC then BP, polyphase planes); 'sweepNR' (NR in 4096, 8192, "

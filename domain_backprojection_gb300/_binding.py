@@ -73,6 +73,9 @@ def load_library(path: str):
         "sar_plan_set_range_window": ([P, ctypes.c_int, I32, ctypes.c_double], ctypes.c_int),
         "sar_plan_set_pulse_weights": ([P, P], ctypes.c_int),
         "sar_plan_kernel_times": ([P, P, P, P, P], ctypes.c_int),
+        "sar_plan_set_accumulation": ([P, ctypes.c_int], ctypes.c_int),
+        "sar_plan_set_stage_precision": ([P, ctypes.c_int], ctypes.c_int),
+        "sar_plan_set_interpolation": ([P, ctypes.c_int], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -292,3 +295,23 @@ def sar_plan_set_pulse_weights(plan: Plan, weights) -> None:
     _check(lib().sar_plan_set_pulse_weights(plan.handle, _dev_tensor(weights, torch.float32, "weights", plan.device)),
            "sar_plan_set_pulse_weights")
     plan.weights = weights
+
+
+SAR_ACCUM_FP32, SAR_ACCUM_COMPENSATED = 0, 1
+SAR_STAGE_FP32, SAR_STAGE_FP16 = 0, 1
+SAR_INTERP_LINEAR, SAR_INTERP_SINC8 = 0, 1
+
+
+def sar_plan_set_accumulation(plan: Plan, accumulation: int) -> None:
+    """SAR_ACCUM_FP32 (plain float32 pulse sums) or SAR_ACCUM_COMPENSATED (batch sums folded into Kahan totals)."""
+    _check(lib().sar_plan_set_accumulation(plan.handle, int(accumulation)), "sar_plan_set_accumulation")
+
+
+def sar_plan_set_stage_precision(plan: Plan, precision: int) -> None:
+    """SAR_STAGE_FP32 or SAR_STAGE_FP16 (float16 staged interpolation entries, float32 arithmetic)."""
+    _check(lib().sar_plan_set_stage_precision(plan.handle, int(precision)), "sar_plan_set_stage_precision")
+
+
+def sar_plan_set_interpolation(plan: Plan, interpolation: int) -> None:
+    """SAR_INTERP_LINEAR or SAR_INTERP_SINC8 (8-tap Hann-tapered sinc, weights normalised to unit sum)."""
+    _check(lib().sar_plan_set_interpolation(plan.handle, int(interpolation)), "sar_plan_set_interpolation")

@@ -36,6 +36,9 @@
 // Per pixel and pulse that leaves: 2 FMA (range offset), 4 FMA (series),
 // 1 add (round), 1 integer op (address), 1 shared 128-bit load, 2 FMA (interp),
 // 1 FMA + sin/cos on the SFU (phase), 4 FMA (complex multiply-accumulate).
+#include <cuda_fp16.h>
+#include <cstring>
+
 #include "sar_internal.cuh"
 
 namespace sar {
@@ -104,6 +107,157 @@ __device__ __forceinline__ void pixel_pulse(const float4 *q4, const int4 wv, con
         acc_r[j] = __ffma2_rn(f2(-vi.x, -vi.y), sn, acc_r[j]);
         acc_i[j] = __ffma2_rn(vr, sn, acc_i[j]);
         acc_i[j] = __ffma2_rn(vi, cs, acc_i[j]);
+    }
+}
+
+__device__ __forceinline__ uint2 lds64(unsigned addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float2 half2_bits_to_float2(unsigned bits)
+{
+    __half2 h;
+    memcpy(&h, &bits, sizeof(h));
+    return __half22float2(h);
+}
+
+// entry address = base + 8 * bits (8-byte entries)
+__device__ __forceinline__ unsigned entry_addr8(unsigned base, float rnd)
+{
+    unsigned a;
+    asm("mad.lo.u32 %0, %1, 8, %2;" : "=r"(a) : "r"(__float_as_uint(rnd)), "r"(base));
+    return a;
+}
+
+// The phase rotation and complex accumulation shared by the variants: acc += (vr + i vi) e^{i ph}.
+__device__ __forceinline__ void rotate_accumulate(const float2 vr, const float2 vi, const float2 ph, float2 &acc_r,
+                                                  float2 &acc_i)
+{
+    float2 sn, cs;
+    __sincosf(ph.x, &sn.x, &cs.x);
+    __sincosf(ph.y, &sn.y, &cs.y);
+    acc_r = __ffma2_rn(vr, cs, acc_r);
+    acc_r = __ffma2_rn(f2(-vi.x, -vi.y), sn, acc_r);
+    acc_i = __ffma2_rn(vr, sn, acc_i);
+    acc_i = __ffma2_rn(vi, cs, acc_i);
+}
+
+// Float16 entries: (m, s) with m = (v_i + v_{i+1}) / 2 and s = v_{i+1} - v_i as two half2
+// (re, im) words.  With r = round(qm), the sample at q = qm + 1/2 is m_r + (qm - r) s_r: the
+// interpolation variable stays within [-1/2, 1/2], so no large intercept (the tau of the float32
+// entries) loses the float16 precision.  Arithmetic in float32.
+template <bool kCheck>
+__device__ __forceinline__ void pixel_pulse_half(const float4 *q4, const int4 wv, const unsigned base, const float2 ox2,
+                                                 const float2 *oyp, const float2 *odp, float2 *acc_r, float2 *acc_i,
+                                                 const BpArgs &args)
+{
+    const float4 Q0 = q4[0], Q1 = q4[1], Q2 = q4[2], Q3 = q4[3];
+    const float2 A2 = f2(Q0.x, Q0.y), B2 = f2(Q0.z, Q0.w), C2 = f2(Q1.x, Q1.y), QM2 = f2(Q1.z, Q1.w);
+    const float2 S1 = f2(Q2.x, Q2.y), S2 = f2(Q2.z, Q2.w), S3 = f2(Q3.x, Q3.y), TH = f2(Q3.z, Q3.w);
+    const float2 half2v = f2(0.5f, 0.5f), magic2 = f2(kRoundMagic, kRoundMagic);
+    const float2 tpk2 = f2(args.two_pi_kappa, args.two_pi_kappa);
+    const float2 adx2 = __fmul2_rn(A2, ox2);
+#pragma unroll
+    for (int j = 0; j < kBpRowsPerThread / 2; j++) {
+        const float2 g = __ffma2_rn(B2, oyp[j], __ffma2_rn(C2, odp[j], adx2));
+        float2 t = __ffma2_rn(g, __ffma2_rn(g, S3, S2), S1);
+        t = __ffma2_rn(g, t, half2v);
+        const float2 qm = __ffma2_rn(g, t, QM2);
+        const float2 rnd = __fadd2_rn(qm, magic2);
+        const float2 ph = __ffma2_rn(qm, tpk2, TH);
+        if (kCheck) {
+            const int e0 = (int)(__float_as_uint(rnd.x) - kRoundMagicBits) + args.wh;
+            const int e1 = (int)(__float_as_uint(rnd.y) - kRoundMagicBits) + args.wh;
+            if (e0 < wv.y || e0 > wv.z || e1 < wv.y || e1 > wv.z) {
+                atomicOr(args.err, kDevErrBounds);
+                continue;
+            }
+        }
+        const float2 fm = __fadd2_rn(qm, f2(kRoundMagic - rnd.x, kRoundMagic - rnd.y));   // qm - round(qm)
+        const uint2 e0 = lds64(entry_addr8(base, rnd.x));
+        const uint2 e1 = lds64(entry_addr8(base, rnd.y));
+        const float2 m0 = half2_bits_to_float2(e0.x), s0 = half2_bits_to_float2(e0.y);
+        const float2 m1 = half2_bits_to_float2(e1.x), s1 = half2_bits_to_float2(e1.y);
+        const float2 vr = f2(fmaf(fm.x, s0.x, m0.x), fmaf(fm.y, s1.x, m1.x));
+        const float2 vi = f2(fmaf(fm.x, s0.y, m0.y), fmaf(fm.y, s1.y, m1.y));
+        rotate_accumulate(vr, vi, ph, acc_r[j], acc_i[j]);
+    }
+}
+
+// 8-tap sinc interpolation.  With q = qm + 1/2, r = floor(q) and f = q - r, taps k = -3 .. 4 read
+// samples r + k with weights proportional to h(f - k), h(d) = sinc(d) (1 + cos(pi d / 4)) / 2 for
+// |d| < 4, normalised to unit sum.  Since sin(pi (f - k)) = (-1)^k sin(pi f), the unnormalised
+// weights are sin(pi f) / pi * (-1)^k W(f - k) / (f - k); the common factor drops out in the
+// normalisation, and so does prod_j (f - j): the weights are proportional to
+//     u_k = (-1)^k W(f - k) prod_{j != k} (f - j),
+// which stays finite at f = 0 (only u_0 is nonzero there: the sample itself).  The taper W(f - k)
+// comes from one sin/cos of pi f / 4 by the angle-sum identity.  Staged entries are float32
+// samples; the row holds three samples before the window and four after.
+template <bool kCheck>
+__device__ __forceinline__ void pixel_pulse_sinc(const float4 *q4, const int4 wv, const unsigned base, const float2 ox2,
+                                                 const float2 *oyp, const float2 *odp, float2 *acc_r, float2 *acc_i,
+                                                 const BpArgs &args)
+{
+    const float4 Q0 = q4[0], Q1 = q4[1], Q2 = q4[2], Q3 = q4[3];
+    const float2 A2 = f2(Q0.x, Q0.y), B2 = f2(Q0.z, Q0.w), C2 = f2(Q1.x, Q1.y), QM2 = f2(Q1.z, Q1.w);
+    const float2 S1 = f2(Q2.x, Q2.y), S2 = f2(Q2.z, Q2.w), S3 = f2(Q3.x, Q3.y), TH = f2(Q3.z, Q3.w);
+    const float2 half2v = f2(0.5f, 0.5f), magic2 = f2(kRoundMagic, kRoundMagic);
+    const float2 tpk2 = f2(args.two_pi_kappa, args.two_pi_kappa);
+    const float2 adx2 = __fmul2_rn(A2, ox2);
+    // (-1)^k cos(pi k / 4) / 2, (-1)^k sin(pi k / 4) / 2 and (-1)^k / 2 for k = -3 .. 4
+    constexpr float r2 = 0.35355339059327376220f;             // sqrt(2) / 4
+    constexpr float kC[8] = {r2, 0.0f, -r2, 0.5f, -r2, 0.0f, r2, -0.5f};
+    constexpr float kS[8] = {r2, -0.5f, r2, 0.0f, -r2, 0.5f, -r2, 0.0f};
+    constexpr float kH[8] = {-0.5f, 0.5f, -0.5f, 0.5f, -0.5f, 0.5f, -0.5f, 0.5f};
+#pragma unroll
+    for (int j = 0; j < kBpRowsPerThread / 2; j++) {
+        const float2 g = __ffma2_rn(B2, oyp[j], __ffma2_rn(C2, odp[j], adx2));
+        float2 t = __ffma2_rn(g, __ffma2_rn(g, S3, S2), S1);
+        t = __ffma2_rn(g, t, half2v);
+        const float2 qm = __ffma2_rn(g, t, QM2);
+        const float2 rnd = __fadd2_rn(qm, magic2);
+        const float2 ph = __ffma2_rn(qm, tpk2, TH);
+        if (kCheck) {
+            const int e0 = (int)(__float_as_uint(rnd.x) - kRoundMagicBits) + args.wh;
+            const int e1 = (int)(__float_as_uint(rnd.y) - kRoundMagicBits) + args.wh;
+            if (e0 < wv.y || e0 > wv.z || e1 < wv.y || e1 > wv.z) {
+                atomicOr(args.err, kDevErrBounds);
+                continue;
+            }
+        }
+        // f = qm + 1/2 - round(qm), in [0, 1]
+        const float2 f = __fadd2_rn(__fadd2_rn(qm, f2(kRoundMagic - rnd.x, kRoundMagic - rnd.y)), half2v);
+        float2 cq, sq;
+        __sincosf(0.78539816339744830962f * f.x, &sq.x, &cq.x);
+        __sincosf(0.78539816339744830962f * f.y, &sq.y, &cq.y);
+        // d_k = f - k; prefix and suffix products of the d's give prod_{j != k} d_j
+        float2 d[8], pre[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) d[k] = __fadd2_rn(f, f2((float)(3 - k), (float)(3 - k)));
+        pre[0] = f2(1.0f, 1.0f);
+#pragma unroll
+        for (int k = 1; k < 8; k++) pre[k] = __fmul2_rn(pre[k - 1], d[k - 1]);
+        float2 suf = f2(1.0f, 1.0f), u[8], sum = f2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 7; k >= 0; k--) {
+            const float2 wk = __ffma2_rn(cq, f2(kC[k], kC[k]), __ffma2_rn(sq, f2(kS[k], kS[k]), f2(kH[k], kH[k])));
+            u[k] = __fmul2_rn(wk, __fmul2_rn(pre[k], suf));
+            suf = __fmul2_rn(suf, d[k]);
+            sum = __fadd2_rn(sum, u[k]);
+        }
+        const unsigned a0 = entry_addr8(base, rnd.x), a1 = entry_addr8(base, rnd.y);
+        float2 v0 = f2(0.0f, 0.0f), v1 = f2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const uint2 s0 = lds64(a0 + 8u * (unsigned)(k - 3)), s1 = lds64(a1 + 8u * (unsigned)(k - 3));
+            v0 = __ffma2_rn(f2(u[k].x, u[k].x), f2(__uint_as_float(s0.x), __uint_as_float(s0.y)), v0);
+            v1 = __ffma2_rn(f2(u[k].y, u[k].y), f2(__uint_as_float(s1.x), __uint_as_float(s1.y)), v1);
+        }
+        const float n0 = __fdividef(1.0f, sum.x), n1 = __fdividef(1.0f, sum.y);
+        rotate_accumulate(f2(v0.x * n0, v1.x * n1), f2(v0.y * n0, v1.y * n1), ph, acc_r[j], acc_i[j]);
     }
 }
 
@@ -271,6 +425,16 @@ __global__ void __launch_bounds__(256) bp_prep_kernel(BpArgs args)
     }
 }
 
+// Kahan's compensated summation of x into (s, c), on a pair of independent sums: c carries the
+// low-order part the previous additions lost, with the sign that makes s - c the better total.
+__device__ __forceinline__ void kahan_add(float2 &s, float2 &c, const float2 x)
+{
+    const float2 y = __fadd2_rn(x, f2(-c.x, -c.y));
+    const float2 t = __fadd2_rn(s, y);
+    c = __fadd2_rn(__fadd2_rn(t, f2(-s.x, -s.y)), f2(-y.x, -y.y));
+    s = t;
+}
+
 __device__ __forceinline__ void cp_async8(unsigned dst, const void *src, int src_bytes)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -287,10 +451,16 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 //   stage  [pulses_per_batch][w] float4 -- the current batch's (tau, sigma) entries.
 // Per batch: issue the copies for batch b+1, prefetch the parameters of batch b+2, run the pixel
 // loop of batch b, then (one barrier later) turn the raw samples of b+1 into (tau, sigma) entries.
-template <int kTileX, bool kCheck, bool kPlanar>
-__global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs args)
+template <int kTileX, bool kCheck, bool kPlanar, int kMode>
+__global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpArgs args)
 {
     constexpr int kTileY = kBpThreads * kBpRowsPerThread / kTileX;
+    // staged entry: (tau, sigma) float4, (m, s) half2 pair, or one float32 sample (sinc rows hold
+    // three samples before the window and four after)
+    constexpr bool kSinc = kMode == kBpSinc8;
+    constexpr unsigned kEb = (kMode == kBpHalfStage || kSinc) ? 8u : 16u;
+    constexpr int kTapsBefore = kSinc ? 3 : 0;
+    constexpr int kExtra = kSinc ? 7 : 1;                       // raw samples per row beyond its entries
     extern __shared__ float4 smem4[];
     constexpr int kWarps = kBpThreads / 32;
     const int pb_cap = args.pulses_per_batch;                                 // parameter slots per batch
@@ -320,6 +490,12 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
     float2 acc_r[kBpRowsPerThread / 2], acc_i[kBpRowsPerThread / 2];
 #pragma unroll
     for (int j = 0; j < kBpRowsPerThread / 2; j++) acc_r[j] = acc_i[j] = f2(0.0f, 0.0f);
+    // compensated variant: the batch sums above are folded after every batch into Kahan totals
+    // (sum, compensation), so rounding grows with the batch length, not the pulse count
+    float2 tot_r[kBpRowsPerThread / 2], tot_i[kBpRowsPerThread / 2], cmp_r[kBpRowsPerThread / 2],
+        cmp_i[kBpRowsPerThread / 2];
+#pragma unroll
+    for (int j = 0; j < kBpRowsPerThread / 2; j++) tot_r[j] = tot_i[j] = cmp_r[j] = cmp_i[j] = f2(0.0f, 0.0f);
 
     const int ns = args.n_samples;
     // this tile's rows of the parameter table, indexed by pulse - pulse_begin
@@ -343,16 +519,17 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
         if (lane == 0) atomicMax(&s_extent, m);
     }
     __syncthreads();
-    const int stride = min(s_extent, args.w);                                // stage entries per row
-    const int rw = (stride + 3) & ~1;                                        // raw samples per row (> stride)
-    const int pb_max = max(1, min(pb_cap, args.stage_bytes / (stride * 16 + rw * 8)));
+    const int stride = min(s_extent, args.w);                                // window entries per row
+    const int row_n = kSinc ? ((stride + kExtra + 1) & ~1) : stride;        // stage entries per row
+    const int rw = (stride + kExtra + 2) & ~1;                               // raw samples per row (even)
+    const int pb_max = max(1, min(pb_cap, args.stage_bytes / (row_n * (int)kEb + rw * 8)));
     float2 *raw = reinterpret_cast<float2 *>(dyn);                           // [pb_max][rw]
-    float4 *stage = dyn + pb_max * rw / 2;                                   // [pb_max][stride]
+    char *stage = reinterpret_cast<char *>(dyn) + (size_t)pb_max * rw * 8;   // [pb_max][row_n] entries
 
-    // entry e of pulse row p lives at stage + p stride + e - e_lo(p); win.w holds p stride - e_lo(p),
-    // and the address of entry round(qm) + wh is formed from the bit pattern of qm + magic with
-    // 32-bit wrap-around
-    const unsigned stage_row0 = (unsigned)__cvta_generic_to_shared(stage) + 16u * (unsigned)wh - 16u * kRoundMagicBits;
+    // entry e of pulse row p lives at stage + p row_n + e - e_lo(p) + kTapsBefore; win.w holds
+    // p row_n - e_lo(p) + kTapsBefore, and the address of entry round(qm) + wh is formed from the bit
+    // pattern of qm + magic with 32-bit wrap-around
+    const unsigned stage_row0 = (unsigned)__cvta_generic_to_shared(stage) + kEb * (unsigned)wh - kEb * kRoundMagicBits;
     const unsigned raw_base = (unsigned)__cvta_generic_to_shared(raw);
 
     // asynchronous gather of batch rows [0, count) starting at pulse n into raw: sample j of row p is
@@ -360,8 +537,8 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
     auto issue_raw = [&](int n, int count, const int4 *win) {
         for (int p = warp; p < count; p += kWarps) {
             const int4 wv = win[p];
-            const int first = wv.x - wh + wv.y;
-            const int nsamp = min(wv.z - wv.y + 2, rw);        // never past the row
+            const int first = wv.x - wh + wv.y - kTapsBefore;
+            const int nsamp = min(wv.z - wv.y + 1 + kExtra, rw);        // never past the row
             const float2 *line = args.rc + (int64_t)(n + p) * ns;
             const unsigned dst = raw_base + (unsigned)(p * rw) * 8u;
             for (int j = lane; j < nsamp; j += 32) {
@@ -373,30 +550,42 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
         }
         cp_async_commit();
     };
-    // raw samples -> (tau, sigma) entries of the staged windows
-    // (pulse n + p of the batch weighted by args.weights[n + p] when the plan has pulse weights)
+    // raw samples -> staged entries: (tau, sigma) float4, (m, s) float16 pairs, or the samples
+    // themselves (sinc); pulse n + p of the batch weighted by args.weights[n + p] when the plan has
+    // pulse weights
     auto transform = [&](int n, int count, const int4 *win) {
         for (int p = warp; p < count; p += kWarps) {
             const int4 wv = win[p];
             const int e_lo = wv.y;
             const int nent = min(wv.z - e_lo + 1, stride);                  // stays inside both rows
             const float2 *rr = raw + p * rw;
-            float4 *row = stage + p * stride;
-            const float im0 = (float)(e_lo - wh) - 0.5f;
-            if (args.weights) {
-                const float wgt = __ldg(args.weights + n + p);
+            const float wgt = args.weights ? __ldg(args.weights + n + p) : 1.0f;
+            if constexpr (kSinc) {
+                float2 *row = reinterpret_cast<float2 *>(stage) + p * row_n;
+                for (int c = lane; c < nent + kExtra; c += 32) {
+                    const float2 v = rr[c];
+                    row[c] = make_float2(wgt * v.x, wgt * v.y);
+                }
+            } else if constexpr (kMode == kBpHalfStage) {
+                uint2 *row = reinterpret_cast<uint2 *>(stage) + p * row_n;
                 for (int c = lane; c < nent; c += 32) {
                     const float2 v0 = rr[c], v1 = rr[c + 1];
-                    const float sr = v1.x - v0.x, si = v1.y - v0.y;
-                    const float im = im0 + (float)c;
-                    row[c] = make_float4(wgt * fmaf(-im, sr, v0.x), wgt * fmaf(-im, si, v0.y), wgt * sr, wgt * si);
+                    const __half2 m = __floats2half2_rn(wgt * 0.5f * (v0.x + v1.x), wgt * 0.5f * (v0.y + v1.y));
+                    const __half2 d = __floats2half2_rn(wgt * (v1.x - v0.x), wgt * (v1.y - v0.y));
+                    uint2 e;
+                    memcpy(&e.x, &m, 4);
+                    memcpy(&e.y, &d, 4);
+                    row[c] = e;
                 }
             } else {
+                float4 *row = reinterpret_cast<float4 *>(stage) + p * row_n;
+                const float im0 = (float)(e_lo - wh) - 0.5f;
                 for (int c = lane; c < nent; c += 32) {
                     const float2 v0 = rr[c], v1 = rr[c + 1];
                     const float sr = v1.x - v0.x, si = v1.y - v0.y;
                     const float im = im0 + (float)c;
-                    row[c] = make_float4(fmaf(-im, sr, v0.x), fmaf(-im, si, v0.y), sr, si);
+                    row[c] = args.weights ? make_float4(wgt * fmaf(-im, sr, v0.x), wgt * fmaf(-im, si, v0.y), wgt * sr, wgt * si)
+                                          : make_float4(fmaf(-im, sr, v0.x), fmaf(-im, si, v0.y), sr, si);
                 }
             }
         }
@@ -408,7 +597,7 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
         quad[4 * p + 2] = make_float4(pc.x, pc.x, pc.y, pc.y);
         quad[4 * p + 3] = make_float4(pc.z, pc.z, pc.w, pc.w);
         const int e_lo = __float_as_int(wf.y);
-        win[p] = make_int4(__float_as_int(wf.x), e_lo, __float_as_int(wf.z), p * stride - e_lo);
+        win[p] = make_int4(__float_as_int(wf.x), e_lo, __float_as_int(wf.z), p * row_n - e_lo + kTapsBefore);
     };
     auto load_params = [&](int n, int count, float4 *quad, int4 *win) {
         if ((int)threadIdx.x < count) {
@@ -450,7 +639,19 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
 #pragma unroll 2
         for (int p = 0; p < pb; p++) {
             const int4 wv = win[p];
-            pixel_pulse<kCheck>(quad + 4 * p, wv, stage_row0 + (unsigned)wv.w * 16u, ox2, oyp, odp, acc_r, acc_i, args);
+            const unsigned base = stage_row0 + (unsigned)wv.w * kEb;
+            if constexpr (kSinc) pixel_pulse_sinc<kCheck>(quad + 4 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
+            else if constexpr (kMode == kBpHalfStage)
+                pixel_pulse_half<kCheck>(quad + 4 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
+            else pixel_pulse<kCheck>(quad + 4 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
+        }
+        if constexpr (kMode == kBpCompensated) {
+#pragma unroll
+            for (int j = 0; j < kBpRowsPerThread / 2; j++) {
+                kahan_add(tot_r[j], cmp_r[j], acc_r[j]);
+                kahan_add(tot_i[j], cmp_i[j], acc_i[j]);
+                acc_r[j] = acc_i[j] = f2(0.0f, 0.0f);
+            }
         }
         if ((int)threadIdx.x < pb2) put_params(threadIdx.x, nx0, nx1, nx2, quads + 4 * pb_cap * buf2, wins + pb_cap * buf2);
         cp_async_wait_all();
@@ -471,6 +672,11 @@ __global__ void __launch_bounds__(kBpThreads, kBpCtasPerSm) bp_kernel(BpArgs arg
         if (ix < args.nx && iy < args.ny) {
             float2 *dst = out + (int64_t)iy * args.nx + ix;
             float2 v = (k & 1) ? make_float2(acc_r[k / 2].y, acc_i[k / 2].y) : make_float2(acc_r[k / 2].x, acc_i[k / 2].x);
+            if constexpr (kMode == kBpCompensated) {
+                // the total less its running compensation (the low part the last additions lost)
+                v = (k & 1) ? make_float2(tot_r[k / 2].y - cmp_r[k / 2].y, tot_i[k / 2].y - cmp_i[k / 2].y)
+                            : make_float2(tot_r[k / 2].x - cmp_r[k / 2].x, tot_i[k / 2].x - cmp_i[k / 2].x);
+            }
             if (direct && args.accumulate) {
                 const float2 old = *dst;
                 v.x += old.x;
@@ -504,16 +710,26 @@ size_t bp_smem_bytes(const BpArgs &a)
     return (size_t)15 * a.pulses_per_batch * sizeof(float4) + (size_t)a.stage_bytes;
 }
 
-template <int TX>
-cudaError_t bp_configure_shape(int smem_bytes)
+template <int TX, int M>
+cudaError_t bp_configure_mode(int smem_bytes)
 {
-    const void *fns[] = {(const void *)bp_kernel<TX, false, false>, (const void *)bp_kernel<TX, false, true>,
-                         (const void *)bp_kernel<TX, true, false>, (const void *)bp_kernel<TX, true, true>};
+    const void *fns[] = {(const void *)bp_kernel<TX, false, false, M>, (const void *)bp_kernel<TX, false, true, M>,
+                         (const void *)bp_kernel<TX, true, false, M>, (const void *)bp_kernel<TX, true, true, M>};
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+template <int TX>
+cudaError_t bp_configure_shape(int smem_bytes)
+{
+    cudaError_t e = bp_configure_mode<TX, kBpLinear>(smem_bytes);
+    if (e == cudaSuccess) e = bp_configure_mode<TX, kBpCompensated>(smem_bytes);
+    if (e == cudaSuccess) e = bp_configure_mode<TX, kBpHalfStage>(smem_bytes);
+    if (e == cudaSuccess) e = bp_configure_mode<TX, kBpSinc8>(smem_bytes);
+    return e;
 }
 
 cudaError_t bp_configure(int smem_bytes)
@@ -524,24 +740,37 @@ cudaError_t bp_configure(int smem_bytes)
     return e;
 }
 
-template <int TX>
-void launch_bp_shape(const BpArgs &a, dim3 grid, size_t smem, bool check_bounds, cudaStream_t s)
+template <int TX, int M>
+void launch_bp_mode(const BpArgs &a, dim3 grid, size_t smem, bool check_bounds, cudaStream_t s)
 {
     if (check_bounds) {
-        if (a.planar) bp_kernel<TX, true, true><<<grid, kBpThreads, smem, s>>>(a);
-        else bp_kernel<TX, true, false><<<grid, kBpThreads, smem, s>>>(a);
+        if (a.planar) bp_kernel<TX, true, true, M><<<grid, kBpThreads, smem, s>>>(a);
+        else bp_kernel<TX, true, false, M><<<grid, kBpThreads, smem, s>>>(a);
     } else {
-        if (a.planar) bp_kernel<TX, false, true><<<grid, kBpThreads, smem, s>>>(a);
-        else bp_kernel<TX, false, false><<<grid, kBpThreads, smem, s>>>(a);
+        if (a.planar) bp_kernel<TX, false, true, M><<<grid, kBpThreads, smem, s>>>(a);
+        else bp_kernel<TX, false, false, M><<<grid, kBpThreads, smem, s>>>(a);
     }
 }
 
-int bp_ctas_per_sm(int smem_bytes)
+template <int TX>
+void launch_bp_shape(const BpArgs &a, dim3 grid, size_t smem, bool check_bounds, cudaStream_t s)
+{
+    switch (a.mode) {
+    case kBpCompensated: launch_bp_mode<TX, kBpCompensated>(a, grid, smem, check_bounds, s); break;
+    case kBpHalfStage: launch_bp_mode<TX, kBpHalfStage>(a, grid, smem, check_bounds, s); break;
+    case kBpSinc8: launch_bp_mode<TX, kBpSinc8>(a, grid, smem, check_bounds, s); break;
+    default: launch_bp_mode<TX, kBpLinear>(a, grid, smem, check_bounds, s); break;
+    }
+}
+
+int bp_ctas_per_sm(int smem_bytes, int mode)
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bp_kernel<128, false, true>, kBpThreads, smem_bytes) !=
-        cudaSuccess)
-        return 1;
+    const void *f = mode == kBpCompensated ? (const void *)bp_kernel<128, false, true, kBpCompensated>
+                    : mode == kBpHalfStage ? (const void *)bp_kernel<128, false, true, kBpHalfStage>
+                    : mode == kBpSinc8     ? (const void *)bp_kernel<128, false, true, kBpSinc8>
+                                           : (const void *)bp_kernel<128, false, true, kBpLinear>;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kBpThreads, smem_bytes) != cudaSuccess) return 1;
     return n > 0 ? n : 1;
 }
 

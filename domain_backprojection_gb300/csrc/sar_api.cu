@@ -24,6 +24,7 @@ struct sar_plan_s {
     // backprojection
     sar::BpArgs bp{};
     int bp_slots = 1;                 // CTAs of bp_kernel resident on the whole device at once
+    int sms = 1;                      // multiprocessors of the plan's device
     int bp_max_slices = 1;            // pulse slices the partial-image buffer can hold
     float2 *d_partial = nullptr;      // [bp_max_slices][ny][nx] partial images
     float4 *d_table = nullptr;        // [tiles][n_pulses] x 48 B per-(tile, pulse) parameters
@@ -339,7 +340,8 @@ sar_status setup_bp(sar_plan p)
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e != cudaSuccess) return cuda_status(e);
-    p->bp_slots = sar::bp_ctas_per_sm(smem) * sms;
+    p->sms = sms;
+    p->bp_slots = sar::bp_ctas_per_sm(smem, a.mode) * sms;
     // partial images for the largest pulse slicing a full-aperture call can pick (at most 512 MB)
     const size_t img_bytes = (size_t)g.nx * g.ny * sizeof(float2);
     int smax = bp_pick_slices(p, r.n_pulses);
@@ -656,6 +658,46 @@ sar_status sar_plan_set_pulse_weights(sar_plan plan, const float *weights)
     if (reinterpret_cast<uintptr_t>(weights) & 3u) return SAR_ERR_INVALID_ARG;
     plan->bp.weights = weights;
     return SAR_OK;
+}
+
+namespace {
+
+// Select variant `mode` for the plan's backprojections, or (to_default) drop it if it is the one
+// selected; refuse to select a second non-default variant.
+sar_status set_bp_mode(sar_plan plan, int mode, bool to_default)
+{
+    if (!plan) return SAR_ERR_INVALID_ARG;
+    if (!plan->has_grid) return SAR_ERR_UNSUPPORTED;
+    int next;
+    if (to_default) next = plan->bp.mode == mode ? sar::kBpLinear : plan->bp.mode;
+    else if (plan->bp.mode == sar::kBpLinear || plan->bp.mode == mode) next = mode;
+    else return SAR_ERR_UNSUPPORTED;
+    if (next == plan->bp.mode) return SAR_OK;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    plan->bp.mode = next;
+    plan->bp_slots = sar::bp_ctas_per_sm((int)sar::bp_smem_bytes(plan->bp), next) * plan->sms;
+    return SAR_OK;
+}
+
+}  // namespace
+
+sar_status sar_plan_set_accumulation(sar_plan plan, sar_accumulation accumulation)
+{
+    if (accumulation != SAR_ACCUM_FP32 && accumulation != SAR_ACCUM_COMPENSATED) return SAR_ERR_INVALID_ARG;
+    return set_bp_mode(plan, sar::kBpCompensated, accumulation == SAR_ACCUM_FP32);
+}
+
+sar_status sar_plan_set_stage_precision(sar_plan plan, sar_stage_precision precision)
+{
+    if (precision != SAR_STAGE_FP32 && precision != SAR_STAGE_FP16) return SAR_ERR_INVALID_ARG;
+    return set_bp_mode(plan, sar::kBpHalfStage, precision == SAR_STAGE_FP32);
+}
+
+sar_status sar_plan_set_interpolation(sar_plan plan, sar_interpolation interpolation)
+{
+    if (interpolation != SAR_INTERP_LINEAR && interpolation != SAR_INTERP_SINC8) return SAR_ERR_INVALID_ARG;
+    return set_bp_mode(plan, sar::kBpSinc8, interpolation == SAR_INTERP_LINEAR);
 }
 
 sar_status sar_plan_set_range_window(sar_plan plan, sar_window window, int32_t taylor_nbar, double taylor_sll_db)

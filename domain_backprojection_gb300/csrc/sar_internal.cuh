@@ -56,6 +56,17 @@ constexpr int kBpThreads = 256;        // threads per CTA: a tile of kBpThreads 
 constexpr int kBpCtasPerSm = 3;        // resident CTAs per SM the kernel is built for (registers, shared memory)
 constexpr int kBpMaxSlices = 32;
 
+// Backprojection variants (one at a time; a plan selects one with its option setters).
+enum BpMode : int {
+    kBpLinear = 0,           // linear interpolation, (tau, sigma) float32 entries, plain float32 sums
+    kBpCompensated = 1,      // as kBpLinear, per-batch sums folded into Kahan-compensated totals
+    kBpHalfStage = 2,        // linear interpolation from float16 (midpoint, slope) entries
+    kBpSinc8 = 3,            // 8-tap Hann-tapered sinc interpolation of float32 samples
+};
+constexpr int kBpModes = 4;
+// Resident CTAs per SM each variant is built for (the heavier variants need more registers).
+constexpr int bp_mode_ctas(int mode) { return mode == kBpLinear || mode == kBpHalfStage ? kBpCtasPerSm : 2; }
+
 struct BpArgs {
     // grid
     double x0, y0, z0;
@@ -91,6 +102,7 @@ struct BpArgs {
     int planar, u_shift, u_mask, n_range;   // planes: sample I of a line at (I & u_mask) Nr + (I >> u_shift)
     const double *pos;       // [Na][3]
     const float *weights;    // [Na] real pulse weights, or null for 1
+    int mode;                // BpMode
     float2 *image;           // [ny][nx]
     int pulse_begin, pulse_end;
     int accumulate;
@@ -99,7 +111,7 @@ struct BpArgs {
 
 size_t bp_smem_bytes(const BpArgs &a);
 cudaError_t bp_configure(int smem_bytes);
-int bp_ctas_per_sm(int smem_bytes);
+int bp_ctas_per_sm(int smem_bytes, int mode);
 // main_begin / main_end (may be null): events recorded on s right around the pixel kernel
 cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s,
                       cudaEvent_t main_begin = nullptr, cudaEvent_t main_end = nullptr);

@@ -205,6 +205,50 @@ sar_status sar_plan_set_range_window(sar_plan plan, sar_window window, int32_t t
  * without a grid. */
 sar_status sar_plan_set_pulse_weights(sar_plan plan, const float *weights);
 
+/* Backprojection variants.  Each option below selects another version of the
+ * pixel kernel for every later backprojection (and image formation) on the
+ * plan.  At most one option differs from its default at a time: setting a
+ * second non-default option returns SAR_ERR_UNSUPPORTED and changes nothing
+ * (reset the first to its default before).  All three return
+ * SAR_ERR_INVALID_ARG for a NULL plan or an unknown value, SAR_ERR_UNSUPPORTED
+ * for a plan without a grid.  None of them launches work. */
+
+/* Accumulation of the pulse sum ("GPU-accelerated backprojection SAR imaging",
+ * sections 2.2 and 4.3: float32 sums over thousands of pulses gather rounding
+ * error; Kahan's compensated summation keeps it small):
+ *   SAR_ACCUM_FP32         plain float32 sums in pulse order (default);
+ *   SAR_ACCUM_COMPENSATED  float32 sums over each staged batch of at most 48
+ *                          pulses, added into a Kahan-compensated running total,
+ *                          so the rounding error grows with the batch length
+ *                          rather than the pulse count. */
+typedef enum { SAR_ACCUM_FP32 = 0, SAR_ACCUM_COMPENSATED = 1 } sar_accumulation;
+sar_status sar_plan_set_accumulation(sar_plan plan, sar_accumulation accumulation);
+
+/* Precision of the compressed samples staged in shared memory ("Fused FFT ->
+ * filter -> IFFT for SAR on Apple Silicon", section 7, on half-precision
+ * storage with single-precision arithmetic):
+ *   SAR_STAGE_FP32  (tau, sigma) float32 interpolation entries (default);
+ *   SAR_STAGE_FP16  each entry holds the midpoint (v_i + v_i+1)/2 and the slope
+ *                   v_i+1 - v_i of the compressed line as float16, halving the
+ *                   staged bytes; arithmetic stays float32.  Compressed samples
+ *                   (times the pulse weights) must stay below 65504 in
+ *                   magnitude, float16's largest finite value. */
+typedef enum { SAR_STAGE_FP32 = 0, SAR_STAGE_FP16 = 1 } sar_stage_precision;
+sar_status sar_plan_set_stage_precision(sar_plan plan, sar_stage_precision precision);
+
+/* Interpolation of the compressed line at each pixel's range ("GPU-accelerated
+ * backprojection SAR imaging", section 2.2: nearest, linear or sinc
+ * interpolation, sinc being the accurate and costly choice):
+ *   SAR_INTERP_LINEAR  linear between the two neighbouring samples (default);
+ *   SAR_INTERP_SINC8   truncated sinc over 8 samples: with q the fractional
+ *                      sample index, r = floor(q) and f = q - r, sample r + k
+ *                      (k = -3 .. 4) has weight h(f - k) / sum_j h(f - j),
+ *                      h(d) = sinc(d) (1 + cos(pi d / 4)) / 2 (a Hann taper
+ *                      that reaches zero at the ends of the 8-sample support).
+ *                      Samples outside the line count as zero. */
+typedef enum { SAR_INTERP_LINEAR = 0, SAR_INTERP_SINC8 = 1 } sar_interpolation;
+sar_status sar_plan_set_interpolation(sar_plan plan, sar_interpolation interpolation);
+
 /* Kernel timing, for benchmarks (no counterpart in the pages).  With enable != 0,
  * each later range-compression call records a pair of CUDA events on its stream
  * around the transform kernel, and each backprojection around the pixel kernel

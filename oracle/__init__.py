@@ -42,6 +42,11 @@ def lib():
                                           ctypes.c_int]
         L.or_backproject.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int64, P,
                                      ctypes.c_int, ctypes.c_int]
+        L.or_backproject_interp.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int64, P,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.or_sinc8_kernel.argtypes = [ctypes.c_double]
+        L.or_sinc8_kernel.restype = ctypes.c_double
+        L.or_interp_line.argtypes = [P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int, P]
         L.or_max_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -101,12 +106,30 @@ def range_compress(radar, raw, upsample=None, threads=0, window=WINDOW_NONE, nba
     return rc
 
 
+INTERP_LINEAR, INTERP_SINC8 = 0, 1
+
+
+def sinc8_kernel(d):
+    """The 8-tap sinc interpolation kernel h(d) (or_sinc8_kernel)."""
+    return float(lib().or_sinc8_kernel(float(d)))
+
+
+def interp_line(line, q, interp=INTERP_LINEAR):
+    """Interpolate one complex line at fractional sample indices q (or_interp_line)."""
+    line = np.ascontiguousarray(line, dtype=np.complex128)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    out = np.zeros(q.shape, dtype=np.complex128)
+    lib().or_interp_line(_ptr(line), line.size, _ptr(q), q.size, int(interp), _ptr(out))
+    return out
+
+
 def backproject(radar, grid, rc, pos, pulse_begin=0, pulse_count=None, pixels=None, out=None,
-                accumulate=False, threads=0):
+                accumulate=False, threads=0, interp=INTERP_LINEAR):
     """rc [pulses][U N] (widened to complex128), pos [pulses][3] float64 -> image.
 
     pixels None: returns the full [ny][nx] complex128 image; otherwise a flat
-    array of the listed pixels (flat index iy * nx + ix)."""
+    array of the listed pixels (flat index iy * nx + ix).  interp: INTERP_LINEAR
+    or INTERP_SINC8."""
     rc = np.ascontiguousarray(rc, dtype=np.complex128)
     pos = np.ascontiguousarray(pos, dtype=np.float64)
     if pulse_count is None:
@@ -120,9 +143,9 @@ def backproject(radar, grid, rc, pos, pulse_begin=0, pulse_count=None, pixels=No
         shape, npix = pix.shape, pix.size
     if out is None:
         out = np.zeros(shape, dtype=np.complex128)
-    lib().or_backproject(ctypes.byref(r), ctypes.byref(_grid(grid)), _ptr(rc), _ptr(pos),
-                         int(pulse_begin), int(pulse_count), None if pix is None else _ptr(pix), npix,
-                         _ptr(out), int(bool(accumulate)), int(threads))
+    lib().or_backproject_interp(ctypes.byref(r), ctypes.byref(_grid(grid)), _ptr(rc), _ptr(pos),
+                                int(pulse_begin), int(pulse_count), None if pix is None else _ptr(pix), npix,
+                                _ptr(out), int(bool(accumulate)), int(interp), int(threads))
     return out
 
 

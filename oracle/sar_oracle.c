@@ -258,16 +258,51 @@ void or_range_compress(const or_radar *r, const float *raw, int64_t n_lines, dou
 
 /* ------------------------------------------------------- backprojection ---- */
 
+/* Kernel of the 8-tap sinc interpolation ("GPU-accelerated backprojection SAR
+ * imaging", section 2.2 names sinc interpolation as the accurate choice; the
+ * truncation length and taper are this oracle's reading):
+ *   h(d) = sinc(d) (1 + cos(pi d / 4)) / 2 for |d| < 4, 0 otherwise,
+ *   sinc(d) = sin(pi d) / (pi d), sinc(0) = 1. */
+double or_sinc8_kernel(double d)
+{
+    if (fabs(d) >= 4.0) return 0.0;
+    const double s = d == 0.0 ? 1.0 : sin(M_PI * d) / (M_PI * d);
+    return s * 0.5 * (1.0 + cos(M_PI * d / 4.0));
+}
+
+/* Sample of line[0 .. un) at fractional index q: interp 0 is the linear
+ * L(q) = (1 - f) line[i] + f line[i + 1]; interp 1 the 8-tap sinc
+ * sum_k h(f - k) line[i + k] / sum_k h(f - k), k = -3 .. 4; with i = floor(q),
+ * f = q - i, and samples outside [0, un) taken as zero. */
+static cplx or_interp(const cplx *line, int64_t un, double q, int interp)
+{
+    const double fi = floor(q);
+    const double f = q - fi;
+    const int64_t i = (int64_t)fi;
+    if (interp == 0) {
+        cplx v0 = (i >= 0 && i < un) ? line[i] : 0.0;
+        cplx v1 = (i + 1 >= 0 && i + 1 < un) ? line[i + 1] : 0.0;
+        return (1.0 - f) * v0 + f * v1;
+    }
+    cplx num = 0.0;
+    double den = 0.0;
+    for (int k = -3; k <= 4; k++) {
+        const double w = or_sinc8_kernel(f - (double)k);
+        den += w;
+        if (i + k >= 0 && i + k < un) num += w * line[i + k];
+    }
+    return num / den;
+}
+
 /* Backproject pulses [pulse_begin, pulse_begin + pulse_count) of rc [pulses][U N]
  * complex128 into pixels.  pixels == NULL means every pixel of the grid in
  * row-major order; otherwise pixels holds n_pix flat indices iy * nx + ix.
  * out[p] = (accumulate ? out[p] : 0) + sum_n L_n(q) exp(+j 4 pi fc R / c0),
- * R = |pixel - a_n|, q = (R - R_start) / dr_U, dr_U = c0 / (2 fs U),
- * L_n(q) = (1 - f) rc_n[i] + f rc_n[i + 1], i = floor(q), f = q - i,
- * samples outside [0, U N) taken as zero. */
-void or_backproject(const or_radar *r, const or_grid *g, const double *rc, const double *pos,
-                    int32_t pulse_begin, int32_t pulse_count, const int64_t *pixels, int64_t n_pix,
-                    double *out, int accumulate, int threads)
+ * R = |pixel - a_n|, q = (R - R_start) / dr_U, dr_U = c0 / (2 fs U), and L_n
+ * the interpolation of line n (or_interp; interp 0 linear, 1 sinc). */
+void or_backproject_interp(const or_radar *r, const or_grid *g, const double *rc, const double *pos,
+                           int32_t pulse_begin, int32_t pulse_count, const int64_t *pixels, int64_t n_pix,
+                           double *out, int accumulate, int interp, int threads)
 {
     const int64_t un = (int64_t)r->upsample * r->n_range;
     const double dr = OR_C0 / (2.0 * r->fs * (double)r->upsample);
@@ -291,17 +326,25 @@ void or_backproject(const or_radar *r, const or_grid *g, const double *rc, const
             double ddx = x - a[0], ddy = y - a[1], ddz = z - a[2];
             double R = sqrt(ddx * ddx + ddy * ddy + ddz * ddz);
             double q = (R - r->range_start) / dr;
-            double fi = floor(q);
-            double f = q - fi;
-            int64_t i = (int64_t)fi;
-            const cplx *line = rcz + (size_t)n * (size_t)un;
-            cplx v0 = (i >= 0 && i < un) ? line[i] : 0.0;
-            cplx v1 = (i + 1 >= 0 && i + 1 < un) ? line[i + 1] : 0.0;
-            cplx val = (1.0 - f) * v0 + f * v1;
+            cplx val = or_interp(rcz + (size_t)n * (size_t)un, un, q, interp);
             acc += val * cexp(I * k4 * R);
         }
         o[p] = accumulate ? o[p] + acc : acc;
     }
+}
+
+/* Linear interpolation (or_backproject_interp with interp 0). */
+void or_backproject(const or_radar *r, const or_grid *g, const double *rc, const double *pos,
+                    int32_t pulse_begin, int32_t pulse_count, const int64_t *pixels, int64_t n_pix,
+                    double *out, int accumulate, int threads)
+{
+    or_backproject_interp(r, g, rc, pos, pulse_begin, pulse_count, pixels, n_pix, out, accumulate, 0, threads);
+}
+
+/* Interpolate line[0 .. un) at the n_q fractional indices q (for the tests). */
+void or_interp_line(const double *line, int64_t un, const double *q, int64_t n_q, int interp, double *out)
+{
+    for (int64_t j = 0; j < n_q; j++) ((cplx *)out)[j] = or_interp((const cplx *)line, un, q[j], interp);
 }
 
 int or_max_threads(void)

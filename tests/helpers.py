@@ -18,7 +18,7 @@ def rel_l2(got, ref):
     return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
 
 
-def oracle_image_pixels(radar, grid, raw, pos, pixels, chunk=2048):
+def oracle_image_pixels(radar, grid, raw, pos, pixels, chunk=2048, interp=oracle.INTERP_LINEAR):
     """Oracle image at the listed flat pixel indices, range-compressing and
     backprojecting the pulses in chunks so that float64 lines never exceed a
     few GB of host memory."""
@@ -30,7 +30,7 @@ def oracle_image_pixels(radar, grid, raw, pos, pixels, chunk=2048):
         n1 = min(na, n0 + chunk)
         rc = oracle.range_compress(radar, raw[n0:n1], threads=ORACLE_THREADS)
         oracle.backproject(radar, grid, rc, pos[n0:n1], pixels=pixels, out=out, accumulate=True,
-                           threads=ORACLE_THREADS)
+                           threads=ORACLE_THREADS, interp=interp)
     return out
 
 

@@ -60,6 +60,9 @@ def test_null_handles():
     assert L.sar_plan_set_timing(None, 1) == 1
     assert L.sar_plan_set_range_window(None, 1, 4, 35.0) == 1
     assert L.sar_plan_set_pulse_weights(None, None) == 1
+    assert L.sar_plan_set_accumulation(None, 1) == 1
+    assert L.sar_plan_set_stage_precision(None, 1) == 1
+    assert L.sar_plan_set_interpolation(None, 1) == 1
     d, i = ctypes.c_double(), ctypes.c_int32()
     assert L.sar_plan_kernel_times(None, ctypes.byref(d), ctypes.byref(i), ctypes.byref(d), ctypes.byref(i)) == 1
 
