@@ -47,6 +47,8 @@ def lib():
         L.or_sinc8_kernel.argtypes = [ctypes.c_double]
         L.or_sinc8_kernel.restype = ctypes.c_double
         L.or_interp_line.argtypes = [P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int, P]
+        L.or_range_doppler.argtypes = [P, ctypes.c_double, P, P, ctypes.c_int, ctypes.c_int]
+        L.or_range_doppler.restype = ctypes.c_int
         L.or_max_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -147,6 +149,21 @@ def backproject(radar, grid, rc, pos, pulse_begin=0, pulse_count=None, pixels=No
                                 int(pulse_begin), int(pulse_count), None if pix is None else _ptr(pix), npix,
                                 _ptr(out), int(bool(accumulate)), int(interp), int(threads))
     return out
+
+
+def range_doppler(radar, rc, pulse_spacing, rcmc=True, threads=0):
+    """Range-Doppler image [Nr][Na] complex128 of range-compressed lines rc [Na][Nr] (upsample 1) from a
+    straight track with `pulse_spacing` metres between pulses (or_range_doppler)."""
+    rc = np.ascontiguousarray(rc, dtype=np.complex128)
+    na, nr = rc.shape
+    r = _radar(radar, upsample=1, n_range=nr)
+    r.n_pulses = na
+    img = np.zeros((nr, na), dtype=np.complex128)
+    st = lib().or_range_doppler(ctypes.byref(r), float(pulse_spacing), _ptr(rc), _ptr(img), int(bool(rcmc)),
+                                int(threads))
+    if st != 0:
+        raise ValueError("pulse spacing too small for the range-Doppler model (lambda / (4 du) >= 1)")
+    return img
 
 
 def form_image(radar, grid, raw, pos, threads=0):

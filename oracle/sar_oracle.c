@@ -18,7 +18,9 @@
  *       4 pi d / lambda, accumulate).
  *   - "Fused FFT -> filter -> IFFT for SAR on Apple Silicon": section 3.1
  *       (range compression per line), section 3.2 (IFFT(x) = conj(FFT(conj x))/N
- *       -- used only by the tests as an identity to pin the FFT here).
+ *       -- used only by the tests as an identity to pin the FFT here), sections
+ *       2.1 and 5.1 (range-Doppler image formation: azimuth DFT, migration
+ *       correction by sinc interpolation, azimuth matched filter, IDFT).
  *   - "Ultra-high-resolution airborne SAR on CUDA": section 5.1 (chirp-z /
  *       Bluestein transform for lengths that are not powers of two).
  *
@@ -345,6 +347,76 @@ void or_backproject(const or_radar *r, const or_grid *g, const double *rc, const
 void or_interp_line(const double *line, int64_t un, const double *q, int64_t n_q, int interp, double *out)
 {
     for (int64_t j = 0; j < n_q; j++) ((cplx *)out)[j] = or_interp((const cplx *)line, un, q[j], interp);
+}
+
+/* ---------------------------------------------------- range-Doppler ---- */
+
+/* Range-Doppler image formation of a straight, uniformly sampled track
+ * ("Fused FFT -> filter -> IFFT for SAR on Apple Silicon", sections 2.1 and
+ * 5.1: range compression, azimuth DFT, range cell migration correction by sinc
+ * interpolation, azimuth matched filter, azimuth IDFT; "Ultra-high-resolution
+ * airborne SAR on CUDA", section 2 names the same three steps).
+ *
+ * rc [Na][Nr] complex128: range-compressed lines at the native spacing
+ * dr = c0 / (2 fs) (upsample 1); du: along-track distance between pulses (m).
+ * img [Nr][Na] complex128: row i is slant range R0 = R_start + i dr, column n
+ * the along-track position of pulse n.
+ *   S(m, i)  = sum_n rc[n][i] exp(-2 pi i m n / Na);
+ *   k_m      = m_s / (Na du) cycles per metre, m_s the signed bin (Nyquist negative);
+ *   D_m      = sqrt(1 - (lambda k_m / 2)^2);
+ *   S'(m, i) = S(m, .) interpolated by the 8-tap sinc at i + R0 (1/D_m - 1) / dr
+ *              (rcmc != 0; otherwise S(m, i) itself);
+ *   S''      = S' exp(+j 4 pi R0 D_m / lambda);
+ *   img[i][n] = (1/Na) sum_m S''(m, i) exp(+2 pi i m n / Na).
+ * Returns 0, or -1 when lambda / (4 du) >= 1 (D_m would not be real). */
+int or_range_doppler(const or_radar *r, double du, const double *rc, double *img, int rcmc, int threads)
+{
+    const int64_t na = r->n_pulses, nr = r->n_range;
+    const double dr = OR_C0 / (2.0 * r->fs);
+    const double lambda = OR_C0 / r->fc;
+    if (!(du > 0.0) || lambda / (4.0 * du) >= 1.0) return -1;
+    const cplx *in = (const cplx *)rc;
+    cplx *out = (cplx *)img;
+    cplx *S = malloc(sizeof(cplx) * (size_t)(na * nr));          /* [Na][Nr]: Doppler bin, range bin */
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#pragma omp parallel for schedule(dynamic, 8)
+#endif
+    for (int64_t i = 0; i < nr; i++) {
+        cplx *col = malloc(sizeof(cplx) * (size_t)na);
+        for (int64_t n = 0; n < na; n++) col[n] = in[n * nr + i];
+        or_dft((double *)col, na, -1);
+        for (int64_t m = 0; m < na; m++) S[m * nr + i] = col[m];
+        free(col);
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 8)
+#endif
+    for (int64_t m = 0; m < na; m++) {
+        const int64_t ms = (2 * m < na) ? m : m - na;
+        const double kx = (double)ms / ((double)na * du);
+        const double D = sqrt(1.0 - (lambda * kx / 2.0) * (lambda * kx / 2.0));
+        cplx *row = malloc(sizeof(cplx) * (size_t)nr);
+        memcpy(row, S + m * nr, sizeof(cplx) * (size_t)nr);
+        for (int64_t i = 0; i < nr; i++) {
+            const double R0 = r->range_start + (double)i * dr;
+            const cplx v = rcmc ? or_interp(row, nr, (double)i + R0 * (1.0 / D - 1.0) / dr, 1) : row[i];
+            S[m * nr + i] = v * cexp(I * 4.0 * M_PI * R0 * D / lambda);
+        }
+        free(row);
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 8)
+#endif
+    for (int64_t i = 0; i < nr; i++) {
+        cplx *col = malloc(sizeof(cplx) * (size_t)na);
+        for (int64_t m = 0; m < na; m++) col[m] = S[m * nr + i];
+        or_dft((double *)col, na, +1);
+        for (int64_t n = 0; n < na; n++) out[i * na + n] = col[n] / (double)na;
+        free(col);
+    }
+    free(S);
+    return 0;
 }
 
 int or_max_threads(void)
