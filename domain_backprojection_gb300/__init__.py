@@ -8,8 +8,9 @@ from ._binding import (SAR_ACCUM_COMPENSATED, SAR_ACCUM_FP32, SAR_INTERP_LINEAR,
                        sar_backproject, sar_form_image, sar_form_image_host, sar_plan_create, sar_plan_destroy,
                        sar_plan_kernel_times, sar_plan_last_launches, sar_plan_set_accumulation,
                        sar_plan_set_interpolation, sar_plan_set_pulse_weights, sar_plan_set_range_window,
-                       sar_plan_set_rc_layout, sar_plan_set_stage_precision, sar_plan_set_timing, sar_plan_sync,
-                       sar_range_compress, sar_status_string, sar_workspace_size)
+                       sar_plan_set_range_doppler, sar_plan_set_rc_layout, sar_plan_set_stage_precision, sar_plan_set_timing,
+                       sar_plan_sync, sar_range_compress, sar_range_doppler, sar_range_doppler_workspace_size,
+                       sar_status_string, sar_workspace_size)
 from .build import build as build_library
 
 __all__ = ["SAR_ACCUM_COMPENSATED", "SAR_ACCUM_FP32", "SAR_INTERP_LINEAR", "SAR_INTERP_SINC8", "SAR_OK",
@@ -18,5 +19,6 @@ __all__ = ["SAR_ACCUM_COMPENSATED", "SAR_ACCUM_FP32", "SAR_INTERP_LINEAR", "SAR_
            "library_path", "sar_backproject", "sar_form_image", "sar_form_image_host", "sar_plan_create",
            "sar_plan_destroy", "sar_plan_kernel_times", "sar_plan_last_launches", "sar_plan_set_accumulation",
            "sar_plan_set_interpolation", "sar_plan_set_pulse_weights", "sar_plan_set_range_window",
-           "sar_plan_set_rc_layout", "sar_plan_set_stage_precision", "sar_plan_set_timing", "sar_plan_sync",
-           "sar_range_compress", "sar_status_string", "sar_workspace_size"]
+           "sar_plan_set_range_doppler", "sar_plan_set_rc_layout", "sar_plan_set_stage_precision", "sar_plan_set_timing",
+           "sar_plan_sync", "sar_range_compress", "sar_range_doppler", "sar_range_doppler_workspace_size",
+           "sar_status_string", "sar_workspace_size"]

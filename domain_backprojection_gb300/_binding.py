@@ -76,6 +76,9 @@ def load_library(path: str):
         "sar_plan_set_accumulation": ([P, ctypes.c_int], ctypes.c_int),
         "sar_plan_set_stage_precision": ([P, ctypes.c_int], ctypes.c_int),
         "sar_plan_set_interpolation": ([P, ctypes.c_int], ctypes.c_int),
+        "sar_plan_set_range_doppler": ([P, ctypes.c_double], ctypes.c_int),
+        "sar_range_doppler_workspace_size": ([P, P], ctypes.c_int),
+        "sar_range_doppler": ([P, P, P, P, SZ, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -315,3 +318,36 @@ def sar_plan_set_stage_precision(plan: Plan, precision: int) -> None:
 def sar_plan_set_interpolation(plan: Plan, interpolation: int) -> None:
     """SAR_INTERP_LINEAR or SAR_INTERP_SINC8 (8-tap Hann-tapered sinc, weights normalised to unit sum)."""
     _check(lib().sar_plan_set_interpolation(plan.handle, int(interpolation)), "sar_plan_set_interpolation")
+
+
+def sar_plan_set_range_doppler(plan: Plan, pulse_spacing: float) -> None:
+    """Azimuth tables for range-Doppler image formation of pulses `pulse_spacing` metres apart."""
+    _check(lib().sar_plan_set_range_doppler(plan.handle, float(pulse_spacing)), "sar_plan_set_range_doppler")
+
+
+def sar_range_doppler_workspace_size(plan: Plan) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().sar_range_doppler_workspace_size(plan.handle, ctypes.byref(n)), "sar_range_doppler_workspace_size")
+    return n.value
+
+
+def sar_range_doppler(plan: Plan, raw: torch.Tensor, image: torch.Tensor = None, workspace: torch.Tensor = None,
+                      stream=None) -> torch.Tensor:
+    """Range-Doppler image [Nr][Na] complex64 of raw [Na][Nr] complex64 (see include/sar.h)."""
+    r = plan.radar
+    if tuple(raw.shape) != (r.n_pulses, r.n_range):
+        raise ValueError(f"raw must be [{r.n_pulses}][{r.n_range}]")
+    ws_bytes = sar_range_doppler_workspace_size(plan)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=raw.device)
+    if workspace.dtype != torch.uint8 or workspace.numel() < ws_bytes or not workspace.is_cuda:
+        raise ValueError(f"workspace must be a CUDA uint8 tensor of at least {ws_bytes} bytes")
+    if image is None:
+        image = torch.empty(r.n_range, r.n_pulses, dtype=torch.complex64, device=raw.device)
+    if tuple(image.shape) != (r.n_range, r.n_pulses):
+        raise ValueError(f"image must be [{r.n_range}][{r.n_pulses}]")
+    _check(lib().sar_range_doppler(plan.handle, _dev_tensor(raw, torch.complex64, "raw", plan.device),
+                                   _dev_tensor(image, torch.complex64, "image", plan.device),
+                                   _dev_tensor(workspace, torch.uint8, "workspace", plan.device),
+                                   workspace.numel(), _stream(stream)), "sar_range_doppler")
+    return image

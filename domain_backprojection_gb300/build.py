@@ -15,8 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libsar.so")
 ROOT = os.path.dirname(HERE)
-SOURCES = ["sar_api.cu", "rc_kernel.cu", "bp_kernel.cu"]
-HEADERS = ["sar_internal.cuh", os.path.join("..", "..", "include", "sar.h")]
+SOURCES = ["sar_api.cu", "rc_kernel.cu", "bp_kernel.cu", "rda_kernel.cu"]
+HEADERS = ["sar_internal.cuh", "fft_reg.cuh", os.path.join("..", "..", "include", "sar.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -29,6 +29,10 @@ struct sar_plan_s {
     float2 *d_partial = nullptr;      // [bp_max_slices][ny][nx] partial images
     float4 *d_table = nullptr;        // [tiles][n_pulses] x 48 B per-(tile, pulse) parameters
     float2 *d_pos_split = nullptr;    // [n_pulses][3] double-float antenna positions
+    // range-Doppler (sar_plan_set_range_doppler): azimuth twiddles | phase coefficients | migration factors
+    sar::RdaArgs rd{};
+    void *d_rd_tables = nullptr;
+    bool rd_ready = false;
     // device error word and its pinned host mirror
     int *d_err = nullptr;
     int *h_err = nullptr;
@@ -394,6 +398,7 @@ void free_plan(sar_plan p)
     cudaFree(p->d_partial);
     cudaFree(p->d_table);
     cudaFree(p->d_pos_split);
+    cudaFree(p->d_rd_tables);
     cudaFree(p->d_err);
     if (p->h_err) cudaFreeHost(p->h_err);
     cudaFree(p->d_raw);
@@ -555,6 +560,85 @@ sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, voi
                              plan->radar.n_pulses, s);
     if (st != SAR_OK) return st;
     return do_backproject(plan, workspace, pos, 0, plan->radar.n_pulses, image, 0, s, SAR_RC_POLYPHASE);
+}
+
+sar_status sar_plan_set_range_doppler(sar_plan plan, double pulse_spacing)
+{
+    if (!plan) return SAR_ERR_INVALID_ARG;
+    const sar_radar &r = plan->radar;
+    const double lambda = kC0 / r.fc;
+    if (!std::isfinite(pulse_spacing) || !(pulse_spacing > 0.0)) return SAR_ERR_INVALID_ARG;
+    if (r.upsample != 1 || !sar::rd_supported_pulses(r.n_pulses)) return SAR_ERR_UNSUPPORTED;
+    if (lambda / (4.0 * pulse_spacing) >= 1.0) return SAR_ERR_UNSUPPORTED;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    const int na = r.n_pulses;
+    // host tables in float64: azimuth twiddles, (2/lambda)(1 - D_m) split into (hi, lo), 1/D_m - 1
+    std::vector<float2> tw(na), phc(na);
+    std::vector<float> rcm(na);
+    for (int t = 0; t < na; t++) {
+        const double ang = -2.0 * M_PI * t / na;
+        tw[t] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        const int ms = (2 * t < na) ? t : t - na;
+        const double kx = (double)ms / ((double)na * pulse_spacing);
+        const double u = lambda * kx / 2.0;
+        const double D = std::sqrt(1.0 - u * u);
+        const double one_minus_d = u * u / (1.0 + D);             // 1 - D without cancellation
+        phc[t] = split_double(2.0 / lambda * one_minus_d);
+        rcm[t] = (float)(one_minus_d / D);                         // 1/D - 1
+    }
+    const size_t bytes = 2 * (size_t)na * sizeof(float2) + (size_t)na * sizeof(float);
+    cudaError_t e = cudaDeviceSynchronize();                        // queued work may read the old tables
+    if (e != cudaSuccess) return cuda_status(e);
+    cudaFree(plan->d_rd_tables);
+    plan->d_rd_tables = nullptr;
+    plan->rd_ready = false;
+    e = cudaMalloc(&plan->d_rd_tables, bytes);
+    char *base = static_cast<char *>(plan->d_rd_tables);
+    if (e == cudaSuccess) e = cudaMemcpy(base, tw.data(), na * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(base + na * sizeof(float2), phc.data(), na * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(base + 2 * na * sizeof(float2), rcm.data(), na * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = sar::rd_configure();
+    if (e != cudaSuccess) return cuda_status(e);
+    sar::RdaArgs &a = plan->rd;
+    a.na = na;
+    a.nr = r.n_range;
+    a.tw = reinterpret_cast<const float2 *>(base);
+    a.phc = reinterpret_cast<const float2 *>(base + na * sizeof(float2));
+    a.rcm = reinterpret_cast<const float *>(base + 2 * na * sizeof(float2));
+    a.range_start = r.range_start;
+    a.dr = kC0 / (2.0 * r.fs);
+    a.two_over_lambda = 2.0 / lambda;
+    a.inv_na = 1.0f / (float)na;
+    plan->rd_ready = true;
+    return SAR_OK;
+}
+
+sar_status sar_range_doppler_workspace_size(sar_plan plan, size_t *bytes)
+{
+    if (!plan || !bytes) return SAR_ERR_INVALID_ARG;
+    if (!plan->rd_ready) return SAR_ERR_UNSUPPORTED;
+    *bytes = 2 * (size_t)plan->radar.n_pulses * plan->radar.n_range * sizeof(float2);
+    return SAR_OK;
+}
+
+sar_status sar_range_doppler(sar_plan plan, const void *raw, void *image, void *workspace, size_t workspace_bytes,
+                             void *stream)
+{
+    if (!plan || !raw || !image || !workspace) return SAR_ERR_INVALID_ARG;
+    if (!plan->rd_ready) return SAR_ERR_UNSUPPORTED;
+    const size_t plane = (size_t)plan->radar.n_pulses * plan->radar.n_range;
+    if (workspace_bytes < 2 * plane * sizeof(float2)) return SAR_ERR_INVALID_ARG;
+    if (!aligned16(raw) || !aligned16(image) || !aligned16(workspace)) return SAR_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (guard.status != cudaSuccess) return SAR_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float2 *rc = static_cast<float2 *>(workspace), *work = rc + plane;
+    plan->last_launches = 4;
+    sar_status st = timed_rc(plan, plan->rc, static_cast<const float2 *>(raw), rc, plan->radar.n_pulses, s);
+    if (st != SAR_OK) return st;
+    return cuda_status(sar::launch_rd(plan->rd, rc, work, static_cast<float2 *>(image), s));
 }
 
 sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double *pos_host, void *image_host,

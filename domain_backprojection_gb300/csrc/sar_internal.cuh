@@ -49,6 +49,23 @@ cudaError_t rc_configure(int n);
 int rc_resident_ctas(int n, int u, int dev);
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s);
 
+// ----------------------------------------------------------- range-Doppler
+struct RdaArgs {
+    int na, nr;              // pulses (the azimuth transform length) and range bins
+    const float2 *tw;        // exp(-2 pi i t / Na), t in [0, Na)
+    const float *rcm;        // [Na] 1 / D_m - 1 (range migration factor), natural Doppler order
+    const float2 *phc;       // [Na] (2 / lambda)(1 - D_m) as (hi, lo) floats, turns per metre of range
+    double range_start;      // m, range of bin 0
+    double dr;               // m, c0 / (2 fs)
+    double two_over_lambda;  // turns per metre
+    float inv_na;            // 1 / Na
+};
+
+bool rd_supported_pulses(int na);
+cudaError_t rd_configure();
+// rc [Na][Nr] compressed lines -> (work [Nr][Na] transposed, then spectra) -> img [Nr][Na]
+cudaError_t launch_rd(const RdaArgs &a, const float2 *rc, float2 *work, float2 *img, cudaStream_t s);
+
 // ----------------------------------------------------------- backprojection
 constexpr int kBpRowsPerThread = 8;   // pixel rows each thread accumulates
 constexpr int kBpThreads = 256;        // threads per CTA: a tile of kBpThreads * kBpRowsPerThread pixels,

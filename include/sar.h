@@ -249,6 +249,46 @@ sar_status sar_plan_set_stage_precision(sar_plan plan, sar_stage_precision preci
 typedef enum { SAR_INTERP_LINEAR = 0, SAR_INTERP_SINC8 = 1 } sar_interpolation;
 sar_status sar_plan_set_interpolation(sar_plan plan, sar_interpolation interpolation);
 
+/* Range-Doppler image formation, a second image-formation path for a straight,
+ * uniformly sampled track ("Fused FFT -> filter -> IFFT for SAR on Apple
+ * Silicon", sections 2.1 and 5.1; "Ultra-high-resolution airborne SAR on
+ * CUDA", section 2): range compression, azimuth DFT of every range bin,
+ * range cell migration correction by interpolation across range bins,
+ * multiplication by the azimuth matched filter, azimuth IDFT.  With dr =
+ * c0 / (2 fs), du the along-track distance between pulses, m the Doppler bin
+ * (m_s its signed value, the Nyquist bin negative), k_m = m_s / (Na du) and
+ * D_m = sqrt(1 - (lambda k_m / 2)^2), output range bin i (R0 = range_start +
+ * i dr) takes the compressed spectrum S(m, .) at range bin
+ * i + R0 (1/D_m - 1) / dr (8-tap sinc interpolation, as SAR_INTERP_SINC8;
+ * bins outside [0, Nr) count as zero), multiplies it by
+ * exp(+j 4 pi R0 D_m / lambda) and transforms back with 1/Na:
+ *   image [Nr][Na] complex64, row i = slant range R0, column n = the
+ *   along-track position of pulse n.
+ * A point target of complex amplitude a focuses at its closest-approach range
+ * and along-track position with phase arg(a) - pi/4 (stationary phase of the
+ * azimuth chirp).  The plan needs upsample 1 and n_pulses a power of two from
+ * 512 to 8192 (SAR_ERR_UNSUPPORTED otherwise). */
+
+/* Build the plan's azimuth tables for pulses `pulse_spacing` metres apart
+ * (finite, > 0: SAR_ERR_INVALID_ARG otherwise; SAR_ERR_UNSUPPORTED when
+ * lambda / (4 pulse_spacing) >= 1, where D_m is not real).  Synchronises the
+ * device first; SAR_ERR_CUDA if an allocation or upload fails. */
+sar_status sar_plan_set_range_doppler(sar_plan plan, double pulse_spacing);
+
+/* Workspace bytes sar_range_doppler needs: 2 Na Nr 8 (the compressed lines and
+ * their transpose).  SAR_ERR_UNSUPPORTED before sar_plan_set_range_doppler. */
+sar_status sar_range_doppler_workspace_size(sar_plan plan, size_t *bytes);
+
+/* Form the range-Doppler image of raw [Na][Nr] complex64 into image [Nr][Na]
+ * complex64, using `workspace` (device, at least
+ * sar_range_doppler_workspace_size bytes, owned by the caller, contents
+ * overwritten).  Four launches on `stream`, no synchronisation.  All device
+ * pointers 16-byte aligned and not overlapping.  SAR_ERR_INVALID_ARG for NULL
+ * or misaligned pointers or a short workspace, SAR_ERR_UNSUPPORTED before
+ * sar_plan_set_range_doppler. */
+sar_status sar_range_doppler(sar_plan plan, const void *raw, void *image, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
 /* Kernel timing, for benchmarks (no counterpart in the pages).  With enable != 0,
  * each later range-compression call records a pair of CUDA events on its stream
  * around the transform kernel, and each backprojection around the pixel kernel

@@ -63,6 +63,9 @@ def test_null_handles():
     assert L.sar_plan_set_accumulation(None, 1) == 1
     assert L.sar_plan_set_stage_precision(None, 1) == 1
     assert L.sar_plan_set_interpolation(None, 1) == 1
+    assert L.sar_plan_set_range_doppler(None, 0.1) == 1
+    assert L.sar_range_doppler_workspace_size(None, ctypes.byref(n)) == 1
+    assert L.sar_range_doppler(None, None, None, None, 0, None) == 1
     d, i = ctypes.c_double(), ctypes.c_int32()
     assert L.sar_plan_kernel_times(None, ctypes.byref(d), ctypes.byref(i), ctypes.byref(d), ctypes.byref(i)) == 1
 
