@@ -277,10 +277,16 @@ def run_ours(args, rank, world, local_rank):
 def rc_kernel_name(nr):
     """The range-compression kernel the library launches for Nr-sample lines: the register-resident
     radix-16 kernel for powers of two from 512 to 8192, the register-resident radix-10/6 kernel for
-    6000, the shared-memory mixed-radix one otherwise."""
+    6000, the shared-memory mixed-radix one for other even 2^a 3^b 5^c lengths, Bluestein otherwise."""
     if nr >= 512 and nr <= 8192 and nr & (nr - 1) == 0:
         return f"rc_reg_kernel<{nr}>"
-    return "rc_mixed6000_kernel" if nr == 6000 else "rc_fused_kernel"
+    if nr == 6000:
+        return "rc_mixed6000_kernel"
+    m = nr
+    for p in (2, 3, 5):
+        while m % p == 0:
+            m //= p
+    return "rc_fused_kernel" if (m == 1 and nr % 2 == 0) else "rc_bluestein_kernel"
 
 
 def profile_case(case="spotlight"):
@@ -419,7 +425,9 @@ def rc_sweep(dev, peaks, reps=20, n_sets=4):
 
     res = {}
     hbm = float(peaks.get("hbm_gbs", 6800.0))
-    for nr in synth.RC_SWEEP_NR:
+    # the range-only lengths, then one length with a prime factor (2 x 23 x 89) that takes the
+    # Bluestein kernel
+    for nr in tuple(synth.RC_SWEEP_NR) + (4094,):
         scene = synth.make_rc_sweep(nr, n_lines=4096, device=dev)
         plan = sar.sar_plan_create(scene["radar"], None, dev.index)
         raws = [scene["raw"]] + [scene["raw"].clone() for _ in range(n_sets - 1)]

@@ -48,20 +48,22 @@ __device__ __forceinline__ void stockham_pass(const float2 *__restrict__ src, fl
     }
 }
 
-// Full forward transform, ping-ponging between a and b; returns the buffer
-// that holds the natural-order result.
-__device__ float2 *dft_forward(float2 *a, float2 *b, const RcArgs &args)
+// Full forward n-point transform (passes of the given radices, twiddles w_n^t),
+// ping-ponging between a and b; returns the buffer that holds the natural-order
+// result.
+__device__ float2 *dft_forward_len(float2 *a, float2 *b, int n, int n_passes, const int *radix,
+                                   const float2 *__restrict__ tw)
 {
     int L = 1;
-    for (int s = 0; s < args.n_passes; s++) {
-        const int r = args.radix[s];
+    for (int s = 0; s < n_passes; s++) {
+        const int r = radix[s];
         switch (r) {
-        case 16: stockham_pass<16>(a, b, args.n, L, args.tw); break;
-        case 8: stockham_pass<8>(a, b, args.n, L, args.tw); break;
-        case 5: stockham_pass<5>(a, b, args.n, L, args.tw); break;
-        case 4: stockham_pass<4>(a, b, args.n, L, args.tw); break;
-        case 3: stockham_pass<3>(a, b, args.n, L, args.tw); break;
-        default: stockham_pass<2>(a, b, args.n, L, args.tw); break;
+        case 16: stockham_pass<16>(a, b, n, L, tw); break;
+        case 8: stockham_pass<8>(a, b, n, L, tw); break;
+        case 5: stockham_pass<5>(a, b, n, L, tw); break;
+        case 4: stockham_pass<4>(a, b, n, L, tw); break;
+        case 3: stockham_pass<3>(a, b, n, L, tw); break;
+        default: stockham_pass<2>(a, b, n, L, tw); break;
         }
         __syncthreads();
         float2 *t = a;
@@ -70,6 +72,87 @@ __device__ float2 *dft_forward(float2 *a, float2 *b, const RcArgs &args)
         L *= r;
     }
     return a;
+}
+
+__device__ float2 *dft_forward(float2 *a, float2 *b, const RcArgs &args)
+{
+    return dft_forward_len(a, b, args.n, args.n_passes, args.radix, args.tw);
+}
+
+// Forward N-point DFT of the N values at `in` (in == A or in == B) by Bluestein's chirp-z
+// identity jk = (j^2 + k^2 - (k - j)^2) / 2 ("Ultra-high-resolution airborne SAR on CUDA",
+// section 5.1): with w_t = exp(-i pi t^2 / N),
+//     X[k] = w_k sum_j (x_j w_j) conj(w_{k-j}),
+// a linear convolution evaluated as an M-point circular one (M >= 2N - 1, a power of two):
+// FFT_M of the zero-padded x w, times Bf = FFT_M(conj w, wrapped) / M (a plan table), then the
+// inverse transform by the conjugate identity.  Returns the buffer (A or B) whose first N entries
+// hold X in natural order.
+__device__ float2 *bluestein_forward(const float2 *in, float2 *A, float2 *B, const RcArgs &args)
+{
+    const int n = args.n, m = args.bm;
+    for (int j = threadIdx.x; j < m; j += blockDim.x)
+        A[j] = j < n ? cmul(in[j], __ldg(args.bw + j)) : make_float2(0.0f, 0.0f);
+    __syncthreads();
+    float2 *P = dft_forward_len(A, B, m, args.bm_passes, args.bm_radix, args.btw);
+    for (int k = threadIdx.x; k < m; k += blockDim.x) P[k] = cconj(cmul(P[k], __ldg(args.bf + k)));
+    __syncthreads();
+    float2 *Q = dft_forward_len(P, P == A ? B : A, m, args.bm_passes, args.bm_radix, args.btw);
+    for (int k = threadIdx.x; k < n; k += blockDim.x) Q[k] = cmul(cconj(Q[k]), __ldg(args.bw + k));
+    __syncthreads();
+    return Q;
+}
+
+// Range compression of lines whose length N has prime factors other than 2, 3 and 5 (or is odd),
+// N <= 4096: every N-point transform of the fused kernel below runs as a Bluestein transform of
+// length M.  Shared memory: two M-entry buffers, plus the N-entry filtered spectrum when U > 1.
+// Plain 8-byte accesses (odd N leaves lines 8-byte aligned only).
+__global__ void __launch_bounds__(512) rc_bluestein_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc,
+                                                           int64_t n_lines, RcArgs args)
+{
+    extern __shared__ float4 smem4[];
+    float2 *sm = reinterpret_cast<float2 *>(smem4);
+    const int n = args.n, U = args.u, m = args.bm;
+    float2 *A = sm, *B = sm + m, *Y = sm + 2 * m;
+    const int un = U * n;
+    const int lo_mask = (1 << args.ptw_lo_bits) - 1;
+    for (int64_t line = blockIdx.x; line < n_lines; line += gridDim.x) {
+        const float2 *src = raw + line * n;
+        for (int j = threadIdx.x; j < n; j += blockDim.x) A[j] = __ldg(src + j);
+        __syncthreads();
+        float2 *X = bluestein_forward(A, A, B, args);
+        float2 *out = rc + line * (int64_t)un;
+        if (U == 1) {
+            for (int k = threadIdx.x; k < n; k += blockDim.x) X[k] = cconj(cmul(X[k], __ldg(args.h + k)));
+            __syncthreads();
+            const float2 *Z = bluestein_forward(X, A, B, args);
+            for (int j = threadIdx.x; j < n; j += blockDim.x) out[j] = cconj(Z[j]);
+            __syncthreads();
+            continue;
+        }
+        for (int k = threadIdx.x; k < n; k += blockDim.x) Y[k] = cmul(X[k], __ldg(args.h + k));
+        __syncthreads();
+        for (int u = 0; u < U; u++) {
+            // conj(Z_u)[k] = conj(Y[k]) * exp(-j 2 pi k_s u / (U Nr)), as in rc_fused_kernel
+            for (int k = threadIdx.x; k < n; k += blockDim.x) {
+                float2 z = cconj(Y[k]);
+                if (u != 0) {
+                    const int ks = (2 * k >= n) ? k - n : k;
+                    int t = (ks * u) % un;
+                    if (t < 0) t += un;
+                    z = cmul(z, cmul(__ldg(args.ptw_hi + (t >> args.ptw_lo_bits)), __ldg(args.ptw_lo + (t & lo_mask))));
+                }
+                A[k] = z;
+            }
+            __syncthreads();
+            const float2 *Z = bluestein_forward(A, A, B, args);
+            if (args.planar) {
+                for (int j = threadIdx.x; j < n; j += blockDim.x) out[(int64_t)u * n + j] = cconj(Z[j]);
+            } else {
+                for (int j = threadIdx.x; j < n; j += blockDim.x) out[(int64_t)U * j + u] = cconj(Z[j]);
+            }
+            __syncthreads();
+        }
+    }
 }
 
 __global__ void __launch_bounds__(512) rc_fused_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc,
@@ -458,6 +541,8 @@ int rc_block_threads(int n) { return n >= 4096 ? 512 : 256; }
 
 size_t rc_smem_bytes(int n, int u) { return (size_t)(u == 1 ? 2 : 3) * n * sizeof(float2); }
 
+size_t rc_bluestein_smem(int n, int u, int m) { return (2 * (size_t)m + (u > 1 ? (size_t)n : 0)) * sizeof(float2); }
+
 namespace {
 
 template <typename K>
@@ -492,6 +577,9 @@ cudaError_t rc_configure(int)
     // every kernel gets its largest shared-memory size, so plans of any size can coexist
     cudaError_t e = cudaFuncSetAttribute(rc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)rc_smem_bytes(8192, 2));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_bluestein_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rc_bluestein_smem(4096, 2, 8192));
     if (e == cudaSuccess) e = set_reg_smem<512, false>();
     if (e == cudaSuccess) e = set_reg_smem<512, true>();
     if (e == cudaSuccess) e = set_reg_smem<1024, false>();
@@ -553,7 +641,12 @@ cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_
         if (a.u == 1) rc_mixed6000_kernel<false><<<grid, 200, rc_mixed_smem(false), s>>>(raw, rc, n_lines, a);
         else rc_mixed6000_kernel<true><<<grid, 200, rc_mixed_smem(true), s>>>(raw, rc, n_lines, a);
         break;
-    default: rc_fused_kernel<<<grid, rc_block_threads(a.n), rc_smem_bytes(a.n, a.u), s>>>(raw, rc, n_lines, a); break;
+    default:
+        if (a.bm > 0)
+            rc_bluestein_kernel<<<grid, 512, rc_bluestein_smem(a.n, a.u, a.bm), s>>>(raw, rc, n_lines, a);
+        else
+            rc_fused_kernel<<<grid, rc_block_threads(a.n), rc_smem_bytes(a.n, a.u), s>>>(raw, rc, n_lines, a);
+        break;
     }
     return cudaGetLastError();
 }

@@ -21,6 +21,7 @@ struct sar_plan_s {
     // range compression
     sar::RcArgs rc{};
     float2 *d_tables = nullptr;       // H | tw | ptw_hi | ptw_lo in one allocation
+    float2 *d_blue = nullptr;         // Bluestein tables (lengths the mixed-radix kernels do not take)
     // backprojection
     sar::BpArgs bp{};
     int bp_slots = 1;                 // CTAs of bp_kernel resident on the whole device at once
@@ -85,6 +86,39 @@ int plan_radices(int n, int *radix)
     for (int r : {16, 8, 4, 5, 3, 2})
         while (n % r == 0 && n > 1) { radix[np++] = r; n /= r; }
     return np;
+}
+
+// Lines the mixed-radix kernels transform directly: even, 2^a 3^b 5^c, up to 8192 samples.  Other
+// lengths from 16 to 4096 go through Bluestein transforms of length M <= 8192.
+bool direct_length(int n) { return n >= 16 && n <= 8192 && (n & 1) == 0 && factor_235(n); }
+bool bluestein_length(int n) { return !direct_length(n) && n >= 16 && n <= 4096; }
+
+// In-place radix-2 DFT of length m (a power of two), sign -1, float64 (host tables only).
+void host_fft(std::vector<double> &re, std::vector<double> &im)
+{
+    const size_t m = re.size();
+    for (size_t i = 1, j = 0; i < m; i++) {
+        size_t bit = m >> 1;
+        for (; j & bit; bit >>= 1) j ^= bit;
+        j ^= bit;
+        if (i < j) {
+            std::swap(re[i], re[j]);
+            std::swap(im[i], im[j]);
+        }
+    }
+    for (size_t len = 2; len <= m; len <<= 1) {
+        for (size_t k = 0; k < len / 2; k++) {
+            const double a = -2.0 * M_PI * (double)k / (double)len, c = std::cos(a), sn = std::sin(a);
+            for (size_t s0 = 0; s0 < m; s0 += len) {
+                const size_t i0 = s0 + k, i1 = i0 + len / 2;
+                const double vr = re[i1] * c - im[i1] * sn, vi = re[i1] * sn + im[i1] * c;
+                re[i1] = re[i0] - vr;
+                im[i1] = im[i0] - vi;
+                re[i0] += vr;
+                im[i0] += vi;
+            }
+        }
+    }
 }
 
 int chirp_samples(const sar_radar &r)
@@ -176,7 +210,7 @@ sar_status validate_radar(const sar_radar *r)
         !std::isfinite(r->range_start))
         return SAR_ERR_INVALID_ARG;
     if (r->n_pulses < 1 || r->n_range < 1 || r->upsample < 1) return SAR_ERR_INVALID_ARG;
-    if (r->n_range < 16 || r->n_range > 8192 || (r->n_range & 1) || !factor_235(r->n_range)) return SAR_ERR_UNSUPPORTED;
+    if (!direct_length(r->n_range) && !bluestein_length(r->n_range)) return SAR_ERR_UNSUPPORTED;
     if (r->upsample != 1 && r->upsample != 2 && r->upsample != 4 && r->upsample != 8) return SAR_ERR_UNSUPPORTED;
     const int nc = chirp_samples(*r);
     if (nc < 1 || nc > r->n_range) return SAR_ERR_UNSUPPORTED;
@@ -233,6 +267,40 @@ sar_status setup_rc(sar_plan p)
     a.ramp = p->d_tables + 2 * n + n_hi + n_lo;
     a.planar = 0;
     a.err = p->d_err;
+    a.bm = 0;
+    if (bluestein_length(n)) {
+        // Bluestein tables: M-point twiddles, w_t = exp(-i pi t^2 / N) (t^2 reduced mod 2N so the
+        // angle stays small), and Bf = FFT_M(b) / M with b_t = conj(w_t) at t and M - t
+        int m = 1;
+        while (m < 2 * n - 1) m <<= 1;
+        a.bm = m;
+        a.bm_passes = plan_radices(m, a.bm_radix);
+        std::vector<float2> bt;
+        for (int t = 0; t < m; t++) {
+            const double ang = -2.0 * M_PI * t / m;
+            bt.push_back(make_float2((float)std::cos(ang), (float)std::sin(ang)));
+        }
+        std::vector<double> br(m, 0.0), bi(m, 0.0);
+        for (int t = 0; t < n; t++) {
+            const long long t2 = ((long long)t * t) % (2LL * n);
+            const double ang = -M_PI * (double)t2 / n;
+            bt.push_back(make_float2((float)std::cos(ang), (float)std::sin(ang)));
+            br[t] = std::cos(ang);
+            bi[t] = -std::sin(ang);
+            if (t > 0) {
+                br[m - t] = br[t];
+                bi[m - t] = bi[t];
+            }
+        }
+        host_fft(br, bi);
+        for (int k = 0; k < m; k++) bt.push_back(make_float2((float)(br[k] / m), (float)(bi[k] / m)));
+        e = cudaMalloc(&p->d_blue, bt.size() * sizeof(float2));
+        if (e == cudaSuccess) e = cudaMemcpy(p->d_blue, bt.data(), bt.size() * sizeof(float2), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_status(e);
+        a.btw = p->d_blue;
+        a.bw = p->d_blue + m;
+        a.bf = p->d_blue + m + n;
+    }
     e = sar::rc_configure(n);
     if (e != cudaSuccess) return cuda_status(e);
     a.max_ctas = sar::rc_resident_ctas(n, U, p->device);
@@ -399,6 +467,7 @@ void free_plan(sar_plan p)
     cudaFree(p->d_table);
     cudaFree(p->d_pos_split);
     cudaFree(p->d_rd_tables);
+    cudaFree(p->d_blue);
     cudaFree(p->d_err);
     if (p->h_err) cudaFreeHost(p->h_err);
     cudaFree(p->d_raw);

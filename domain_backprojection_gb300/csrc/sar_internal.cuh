@@ -37,6 +37,13 @@ struct RcArgs {
     const float2 *ptw_lo;    // exp(-2 pi i lo / (U Nr)), lo < 2^bits
     const float2 *ramp;      // exp(+2 pi i k_s / (U Nr)) for k in [0, Nr), k_s the signed frequency
     int planar;              // output layout: 0 natural (sample U m + u at U m + u), 1 planes (at u Nr + m)
+    // Bluestein transforms (lengths other than 2^a 3^b 5^c, or odd): bm = 0 when unused
+    int bm;                  // convolution length M (a power of two >= 2 Nr - 1)
+    int bm_passes;
+    int bm_radix[kMaxPasses];
+    const float2 *btw;       // exp(-2 pi i t / M), t in [0, M)
+    const float2 *bw;        // exp(-i pi t^2 / Nr), t in [0, Nr)
+    const float2 *bf;        // FFT_M of the wrapped conj(bw), divided by M
     int max_ctas;            // CTAs of the line kernel resident on the whole device (its grid cap)
     int *err;                // device error word
 };
@@ -44,6 +51,7 @@ struct RcArgs {
 int rc_block_threads(int n);
 bool rc_has_reg_path(int n);
 size_t rc_smem_bytes(int n, int u);
+size_t rc_bluestein_smem(int n, int u, int m);
 cudaError_t rc_configure(int n);
 // CTAs of the line kernel for (n, u) that fit on device `dev` at once (0 on error).
 int rc_resident_ctas(int n, int u, int dev);

@@ -73,10 +73,11 @@ def test_null_handles():
 @pytest.mark.parametrize("change,expect", [
     (dict(fs=-1.0), 1), (dict(fc=math.nan), 1), (dict(range_start=math.inf), 1), (dict(bandwidth=0.0), 1),
     (dict(n_pulses=0), 1), (dict(upsample=0), 1),
-    (dict(n_range=1026), 2),        # 2 * 3^3 * 19: not 2^a 3^b 5^c
-    (dict(n_range=8190), 2),        # 2 * 3^2 * 5 * 7 * 13
+    (dict(n_range=8190), 2),        # 2 * 3^2 * 5 * 7 * 13: beyond the Bluestein limit (4096)
+    (dict(n_range=4098), 2),        # 2 * 3 * 683: beyond the Bluestein limit
+    (dict(n_range=4097), 2),        # odd, beyond the Bluestein limit
     (dict(n_range=16384), 2),       # beyond the on-chip line
-    (dict(n_range=375), 2),         # odd
+    (dict(n_range=15), 2),          # below 16
     (dict(upsample=3), 2), (dict(upsample=16), 2),
     (dict(n_range=256), 2),         # the 360-sample pulse does not fit the line
 ])
@@ -90,6 +91,14 @@ def test_invalid_grid_and_outputs():
     assert _create(grid=dataclasses.replace(GRID, nx=0)) == 1
     assert _create(grid=dataclasses.replace(GRID, dy=-0.5)) == 1
     assert _create(grid=dataclasses.replace(GRID, x0=math.nan)) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+@pytest.mark.parametrize("n_range", [1026, 375, 1009, 4096, 6000])
+def test_bluestein_and_direct_lengths_pass_validation(n_range):
+    # 2 * 3^3 * 19, odd 3 * 5^3 and the prime 1009 go through Bluestein transforms; validation
+    # accepts them, so plan creation gets as far as the device (and fails there without a GPU)
+    assert _create(dataclasses.replace(RADAR, n_range=n_range)) == 4
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")

@@ -38,6 +38,8 @@ def _run(radar, raw_cpu):
     (16, 1, 3), (16, 8, 2), (30, 2, 5), (240, 4, 7), (1000, 1, 9), (1000, 8, 3), (1536, 2, 4),
     (1024, 1, 1), (1024, 8, 37), (2048, 8, 64), (4096, 1, 100), (4096, 1, 7), (4096, 1, 1), (4096, 8, 16),
     (6000, 1, 50), (6000, 8, 5), (8192, 1, 33), (8192, 1, 2), (8192, 8, 9), (8192, 4, 3), (4050, 2, 3),
+    # Bluestein lengths: 2 * 3^3 * 19, the prime 1009, odd 3 * 5^3, 2 * 23 * 89, the largest odd
+    (1026, 1, 5), (1026, 8, 3), (1009, 2, 4), (375, 1, 3), (375, 4, 2), (4094, 4, 2), (4095, 1, 2),
 ])
 def test_rc_random_lines(n, U, lines):
     radar = _short_pulse_radar(n, U, lines) if n < 400 else synth.Radar(range_start=5000.0, n_pulses=lines,
@@ -159,3 +161,21 @@ def test_range_window_bad_arguments():
     assert L.sar_plan_set_range_window(plan.handle, sar.SAR_WINDOW_TAYLOR, 4, 0.0) == 1
     assert L.sar_plan_set_range_window(plan.handle, sar.SAR_WINDOW_TAYLOR, 4, float("nan")) == 1
     assert L.sar_plan_set_range_window(plan.handle, sar.SAR_WINDOW_HAMMING, 0, 0.0) == 0
+
+
+def test_image_from_bluestein_length_lines():
+    # a whole image whose lines (1026 samples) go through the Bluestein kernel: range compression
+    # (U = 8, natural and polyphase layouts) and backprojection against the oracle
+    import dataclasses
+    from helpers import IMG_TOL
+    cfg = dataclasses.replace(synth.CONFIGS[1], n_pulses=96, prf=300.0 * 96 / 256, n_range=1026, nx=45, ny=70,
+                              fixed_target_offsets=((0, 0), (-9, 11), (13, -20)))
+    s = synth.make_scene(cfg, device="cuda")
+    plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
+    img = sar.sar_form_image(plan, s["raw"], s["pos"])
+    rc = sar.sar_range_compress(plan, s["raw"])
+    sar.sar_plan_sync(plan)
+    ref_rc = oracle.range_compress(s["radar"], s["raw"].cpu().numpy(), threads=ORACLE_THREADS)
+    assert rel_l2(rc.cpu().numpy(), ref_rc) <= RC_TOL
+    ref = oracle.backproject(s["radar"], s["grid"], ref_rc, s["pos"].cpu().numpy(), threads=ORACLE_THREADS)
+    assert rel_l2(img.cpu().numpy(), ref) <= IMG_TOL
