@@ -274,10 +274,11 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
-def rc_kernel_name(nr):
+def rc_kernel_name(nr, upsample=1):
     """The range-compression kernel the library launches for Nr-sample lines: the register-resident
     radix-16 kernel for powers of two from 512 to 8192, the register-resident radix-10/6 kernel for
-    6000, the shared-memory mixed-radix one for other even 2^a 3^b 5^c lengths, Bluestein otherwise."""
+    6000, the shared-memory mixed-radix one for other even 2^a 3^b 5^c lengths, Bluestein otherwise
+    (register-resident without upsampling, in shared memory with it)."""
     if nr >= 512 and nr <= 8192 and nr & (nr - 1) == 0:
         return f"rc_reg_kernel<{nr}>"
     if nr == 6000:
@@ -286,7 +287,12 @@ def rc_kernel_name(nr):
     for p in (2, 3, 5):
         while m % p == 0:
             m //= p
-    return "rc_fused_kernel" if (m == 1 and nr % 2 == 0) else "rc_bluestein_kernel"
+    if m == 1 and nr % 2 == 0:
+        return "rc_fused_kernel"
+    bm = 512
+    while bm < 2 * nr - 1:
+        bm *= 2
+    return f"rc_blue_reg_kernel<{bm}>" if upsample == 1 else "rc_bluestein_kernel"
 
 
 def profile_case(case="spotlight"):

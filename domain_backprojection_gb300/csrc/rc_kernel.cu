@@ -535,6 +535,63 @@ __global__ void __launch_bounds__(200, kMulti ? kRcMixedCtas : 2) rc_mixed6000_k
     }
 }
 
+// Bluestein lines without upsampling, register-resident: the four M-point transforms of a line
+// (M = 512 .. 8192) are reg_dft passes over the thread's 16 elements t + T p (T = M / 16), the
+// line's samples in the first N positions.
+template <int M>
+constexpr int rc_blue_min_ctas() { return M >= 8192 ? 1 : M == 4096 ? 2 : (16 * 32) / (M / 16); }
+
+template <int M>
+__global__ void __launch_bounds__(M / 16, rc_blue_min_ctas<M>())
+    rc_blue_reg_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc, int64_t n_lines, RcArgs args)
+{
+    extern __shared__ float4 smem4[];
+    constexpr int T = M / 16;
+    float2 *a = reinterpret_cast<float2 *>(smem4), *b = a;
+    const int t = threadIdx.x, n = args.n;
+    for (int64_t line = blockIdx.x; line < n_lines; line += gridDim.x) {
+        const float2 *src = raw + line * n;
+        float2 x[16];
+#pragma unroll
+        for (int p = 0; p < 16; p++) {
+            const int k = t + T * p;
+            x[p] = k < n ? cmul(__ldg(src + k), __ldg(args.bw + k)) : make_float2(0.0f, 0.0f);
+        }
+        // four transforms, one copy of the transform code: after transforms 0 and 2 the convolution
+        // spectrum is multiplied by Bf (and conjugated for the inverse), after transform 1 the line's
+        // spectrum X is filtered and prepared for the inverse Bluestein transform
+#pragma unroll 1
+        for (int trip = 0; trip < 4; trip++) {
+            reg_dft<M, false>(x, a, b, args.btw);
+            if (trip == 1) {
+#pragma unroll
+                for (int p = 0; p < 16; p++) {
+                    const int k = t + T * p;
+                    if (k < n) {
+                        const float2 w = __ldg(args.bw + k);
+                        const float2 X = cmul(w, cconj(x[p]));                   // spectrum bin k
+                        x[p] = cmul(cconj(cmul(X, __ldg(args.h + k))), w);      // conj(X H) w
+                    } else {
+                        x[p] = make_float2(0.0f, 0.0f);
+                    }
+                }
+            } else if (trip != 3) {
+#pragma unroll
+                for (int p = 0; p < 16; p++) x[p] = cconj(cmul(x[p], __ldg(args.bf + t + T * p)));
+            }
+        }
+        float2 *out = rc + line * (int64_t)n;
+#pragma unroll
+        for (int p = 0; p < 16; p++) {
+            const int k = t + T * p;
+            if (k < n) out[k] = cconj(cmul(__ldg(args.bw + k), cconj(x[p])));
+        }
+    }
+}
+
+template <int M>
+size_t rc_blue_reg_smem() { return (size_t)(M + M / 16) * sizeof(float2); }
+
 }  // namespace
 
 int rc_block_threads(int n) { return n >= 4096 ? 512 : 256; }
@@ -580,6 +637,12 @@ cudaError_t rc_configure(int)
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(rc_bluestein_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)rc_bluestein_smem(4096, 2, 8192));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_blue_reg_kernel<4096>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rc_blue_reg_smem<4096>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_blue_reg_kernel<8192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rc_blue_reg_smem<8192>());
     if (e == cudaSuccess) e = set_reg_smem<512, false>();
     if (e == cudaSuccess) e = set_reg_smem<512, true>();
     if (e == cudaSuccess) e = set_reg_smem<1024, false>();
@@ -642,7 +705,15 @@ cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_
         else rc_mixed6000_kernel<true><<<grid, 200, rc_mixed_smem(true), s>>>(raw, rc, n_lines, a);
         break;
     default:
-        if (a.bm > 0)
+        if (a.bm > 0 && a.u == 1) {
+            switch (a.bm) {
+            case 512: rc_blue_reg_kernel<512><<<grid, 32, rc_blue_reg_smem<512>(), s>>>(raw, rc, n_lines, a); break;
+            case 1024: rc_blue_reg_kernel<1024><<<grid, 64, rc_blue_reg_smem<1024>(), s>>>(raw, rc, n_lines, a); break;
+            case 2048: rc_blue_reg_kernel<2048><<<grid, 128, rc_blue_reg_smem<2048>(), s>>>(raw, rc, n_lines, a); break;
+            case 4096: rc_blue_reg_kernel<4096><<<grid, 256, rc_blue_reg_smem<4096>(), s>>>(raw, rc, n_lines, a); break;
+            default: rc_blue_reg_kernel<8192><<<grid, 512, rc_blue_reg_smem<8192>(), s>>>(raw, rc, n_lines, a); break;
+            }
+        } else if (a.bm > 0)
             rc_bluestein_kernel<<<grid, 512, rc_bluestein_smem(a.n, a.u, a.bm), s>>>(raw, rc, n_lines, a);
         else
             rc_fused_kernel<<<grid, rc_block_threads(a.n), rc_smem_bytes(a.n, a.u), s>>>(raw, rc, n_lines, a);

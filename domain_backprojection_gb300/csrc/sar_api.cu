@@ -271,7 +271,7 @@ sar_status setup_rc(sar_plan p)
     if (bluestein_length(n)) {
         // Bluestein tables: M-point twiddles, w_t = exp(-i pi t^2 / N) (t^2 reduced mod 2N so the
         // angle stays small), and Bf = FFT_M(b) / M with b_t = conj(w_t) at t and M - t
-        int m = 1;
+        int m = 512;                                            // the register transforms start at 512
         while (m < 2 * n - 1) m <<= 1;
         a.bm = m;
         a.bm_passes = plan_radices(m, a.bm_radix);
