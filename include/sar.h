@@ -57,7 +57,10 @@ typedef struct {
     double fs;            /* complex sampling rate, Hz (> 0) */
     double range_start;   /* slant range of sample 0, m */
     int32_t n_pulses;     /* pulses Na (>= 1) */
-    int32_t n_range;      /* samples per pulse Nr: even, of the form 2^a 3^b 5^c, 16 <= Nr <= 8192 */
+    int32_t n_range;      /* samples per pulse Nr: 16 <= Nr <= 8192 when even and of the form
+                             2^a 3^b 5^c (mixed-radix transforms); any other 16 <= Nr <= 4096
+                             (Bluestein / chirp-z transforms, "Ultra-high-resolution airborne
+                             SAR on CUDA", section 5.1) */
     int32_t upsample;     /* range upsampling U in {1, 2, 4, 8} */
 } sar_radar;
 
