@@ -121,17 +121,20 @@ __global__ void __launch_bounds__(N / 16, rd_min_ctas<N>()) rd_compress_kernel(c
             const float q = (float)i + r_bins * __ldg(args.rcm + m);
             const float fl = floorf(q);
             const int r0 = (int)fl - 3;
+            // the eight taps first (rows clamped into the axis, so every load is in bounds and none
+            // waits on a branch), the weights while they are in flight; taps outside the axis
+            // weigh zero
+            float2 sv[8];
+#pragma unroll
+            for (int k = 0; k < 8; k++) sv[k] = __ldg(s + (int64_t)min(max(r0 + k, 0), nr - 1) * N + m);
             float w[8];
             sinc8_weights(q - fl, w);
             float2 v = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int k = 0; k < 8; k++) {
-                const int r = r0 + k;
-                if (r >= 0 && r < nr) {
-                    const float2 sv = __ldg(s + (int64_t)r * N + m);
-                    v.x = fmaf(w[k], sv.x, v.x);
-                    v.y = fmaf(w[k], sv.y, v.y);
-                }
+                const float wk = (r0 + k >= 0 && r0 + k < nr) ? w[k] : 0.0f;
+                v.x = fmaf(wk, sv[k].x, v.x);
+                v.y = fmaf(wk, sv[k].y, v.y);
             }
             // matched filter phase, turns: frac((2/lambda) R0) - (2/lambda)(1 - D_m) R0 (double-float)
             const float2 c = __ldg(args.phc + m);
