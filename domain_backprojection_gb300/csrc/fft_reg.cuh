@@ -356,15 +356,30 @@ __device__ __forceinline__ unsigned long long global_ns()
     return t;
 }
 
-// Wait for the barrier phase of the given parity; false if kWaitLimitNs (or an iteration cap)
-// passed first.
-__device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity)
+// Non-blocking test of the barrier phase of the given parity.
+__device__ __forceinline__ bool stage_test_wait(uint64_t *bar, uint32_t parity)
 {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+
+// Wait for the barrier phase of the given parity; false if limit_ns (or an iteration cap) passed
+// first.  limit_ns = 0 tests the phase once without waiting (the plan's wait-limit knob, which
+// lets a test make the wait run out).
+__device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity, unsigned long long limit_ns)
+{
+    if (limit_ns == 0) return stage_test_wait(bar, parity);
     if (stage_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 0; i < (1u << 30); i++) {
         if (stage_try_wait(bar, parity)) return true;
-        if ((i & 63) == 63 && global_ns() - t0 > kWaitLimitNs) break;
+        if ((i & 63) == 63 && global_ns() - t0 > limit_ns) break;
     }
     return false;
 }

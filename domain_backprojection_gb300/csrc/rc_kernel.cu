@@ -331,13 +331,17 @@ __global__ void __launch_bounds__(N / 16, (rc_reg_min_ctas<N, kMulti>()))
         if (t == 0) stage_line(bar, stage, raw + line * N, N * sizeof(float2));
         uint32_t parity = 0;
         for (; line < n_lines; line += gridDim.x) {
-            const bool ok = stage_wait(bar, parity);
+            const uint32_t ph = parity;
+            const bool ok = stage_wait(bar, ph, args.wait_limit_ns);
             parity ^= 1u;
             float2 x[16];
 #pragma unroll
             for (int p = 0; p < 16; p++) x[p] = stage[t + T * p];
             if (__syncthreads_or(!ok)) {                        // the stage is free again (or the copy never came)
-                if (t == 0) atomicOr(args.err, kDevErrTimeout);
+                if (t == 0) {
+                    atomicOr(args.err, kDevErrTimeout);
+                    stage_wait(bar, ph, kWaitLimitNs);          // let the copy in flight land before the CTA exits
+                }
                 return;
             }
             if (t == 0 && line + gridDim.x < n_lines)
@@ -519,13 +523,17 @@ __global__ void __launch_bounds__(200, kMulti ? kRcMixedCtas : 2) rc_mixed6000_k
         if (t == 0) stage_line(bar, stage, raw + line * N, N * sizeof(float2));
         uint32_t parity = 0;
         for (; line < n_lines; line += gridDim.x) {
-            const bool ok = stage_wait(bar, parity);
+            const uint32_t ph = parity;
+            const bool ok = stage_wait(bar, ph, args.wait_limit_ns);
             parity ^= 1u;
             float2 x[E];
 #pragma unroll
             for (int p = 0; p < E; p++) x[p] = stage[t + T * p];
             if (__syncthreads_or(!ok)) {
-                if (t == 0) atomicOr(args.err, kDevErrTimeout);
+                if (t == 0) {
+                    atomicOr(args.err, kDevErrTimeout);
+                    stage_wait(bar, ph, kWaitLimitNs);          // let the copy in flight land before the CTA exits
+                }
                 return;
             }
             if (t == 0 && line + gridDim.x < n_lines)

@@ -71,6 +71,27 @@ struct DeviceGuard {
 bool finite_pos(double v) { return std::isfinite(v) && v > 0.0; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Fault-injection hook for tests: with SAR_INJECT_ALLOC_FAILURE=1 in the environment every device
+// allocation the library makes reports cudaErrorMemoryAllocation without calling CUDA, so the
+// SAR_ERR_NO_MEMORY paths (and the clean-up behind them) run on any machine.
+cudaError_t dev_alloc(void **p, size_t bytes)
+{
+    const char *inj = std::getenv("SAR_INJECT_ALLOC_FAILURE");
+    if (inj && inj[0] == '1') {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+}
+template <typename T>
+cudaError_t dev_alloc(T **p, size_t bytes)
+{
+    void *v = nullptr;
+    const cudaError_t e = dev_alloc(&v, bytes);
+    *p = static_cast<T *>(v);
+    return e;
+}
+
 bool factor_235(int n)
 {
     for (int p : {2, 3, 5})
@@ -256,7 +277,7 @@ sar_status setup_rc(sar_plan p)
         const double ang = 2.0 * M_PI * (double)ks / un;
         host.push_back(make_float2((float)std::cos(ang), (float)std::sin(ang)));
     }
-    cudaError_t e = cudaMalloc(&p->d_tables, host.size() * sizeof(float2));
+    cudaError_t e = dev_alloc(&p->d_tables, host.size() * sizeof(float2));
     if (e != cudaSuccess) return cuda_status(e);
     e = cudaMemcpy(p->d_tables, host.data(), host.size() * sizeof(float2), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_status(e);
@@ -267,6 +288,8 @@ sar_status setup_rc(sar_plan p)
     a.ramp = p->d_tables + 2 * n + n_hi + n_lo;
     a.planar = 0;
     a.err = p->d_err;
+    a.wait_limit_ns = sar::kWaitLimitNs;
+    if (const char *wl = std::getenv("SAR_WAIT_LIMIT_NS")) a.wait_limit_ns = std::strtoull(wl, nullptr, 10);
     a.bm = 0;
     if (bluestein_length(n)) {
         // Bluestein tables: M-point twiddles, w_t = exp(-i pi t^2 / N) (t^2 reduced mod 2N so the
@@ -294,7 +317,7 @@ sar_status setup_rc(sar_plan p)
         }
         host_fft(br, bi);
         for (int k = 0; k < m; k++) bt.push_back(make_float2((float)(br[k] / m), (float)(bi[k] / m)));
-        e = cudaMalloc(&p->d_blue, bt.size() * sizeof(float2));
+        e = dev_alloc(&p->d_blue, bt.size() * sizeof(float2));
         if (e == cudaSuccess) e = cudaMemcpy(p->d_blue, bt.data(), bt.size() * sizeof(float2), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_status(e);
         a.btw = p->d_blue;
@@ -400,8 +423,8 @@ sar_status setup_bp(sar_plan p)
     a.err = p->d_err;
     {
         const size_t entries = (size_t)a.tiles_x * a.tiles_y * r.n_pulses;
-        cudaError_t et = cudaMalloc(&p->d_table, entries * 3 * sizeof(float4));
-        if (et == cudaSuccess) et = cudaMalloc(&p->d_pos_split, (size_t)r.n_pulses * 3 * sizeof(float2));
+        cudaError_t et = dev_alloc(&p->d_table, entries * 3 * sizeof(float4));
+        if (et == cudaSuccess) et = dev_alloc(&p->d_pos_split, (size_t)r.n_pulses * 3 * sizeof(float2));
         if (et != cudaSuccess) return cuda_status(et);
         a.table = p->d_table;
         a.pos_split = p->d_pos_split;
@@ -420,7 +443,7 @@ sar_status setup_bp(sar_plan p)
     while (smax > 1 && (size_t)smax * img_bytes > ((size_t)512 << 20)) smax--;
     p->bp_max_slices = smax;
     if (smax > 1) {
-        e = cudaMalloc(&p->d_partial, (size_t)smax * img_bytes);
+        e = dev_alloc(&p->d_partial, (size_t)smax * img_bytes);
         if (e != cudaSuccess) return cuda_status(e);
     }
     return SAR_OK;
@@ -543,7 +566,7 @@ sar_status sar_plan_create(const sar_radar *radar, const sar_grid *grid, int dev
     }
     const char *cb = std::getenv("SAR_CHECK_BOUNDS");
     p->check_bounds = cb && cb[0] == '1';
-    cudaError_t e = cudaMalloc(&p->d_err, sizeof(int));
+    cudaError_t e = dev_alloc(&p->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMallocHost(&p->h_err, sizeof(int));
     if (e != cudaSuccess) {
@@ -662,7 +685,7 @@ sar_status sar_plan_set_range_doppler(sar_plan plan, double pulse_spacing)
     cudaFree(plan->d_rd_tables);
     plan->d_rd_tables = nullptr;
     plan->rd_ready = false;
-    e = cudaMalloc(&plan->d_rd_tables, bytes);
+    e = dev_alloc(&plan->d_rd_tables, bytes);
     char *base = static_cast<char *>(plan->d_rd_tables);
     if (e == cudaSuccess) e = cudaMemcpy(base, tw.data(), na * sizeof(float2), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(base + na * sizeof(float2), phc.data(), na * sizeof(float2), cudaMemcpyHostToDevice);
@@ -724,10 +747,10 @@ sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double
     size_t ws = 0;
     sar_workspace_size(plan, &ws);
     cudaError_t e = cudaSuccess;
-    if (!plan->d_raw && e == cudaSuccess) e = cudaMalloc(&plan->d_raw, raw_bytes);
-    if (!plan->d_pos && e == cudaSuccess) e = cudaMalloc(&plan->d_pos, pos_bytes);
-    if (!plan->d_rc && e == cudaSuccess) e = cudaMalloc(&plan->d_rc, ws);
-    if (!plan->d_img && e == cudaSuccess) e = cudaMalloc(&plan->d_img, img_bytes);
+    if (!plan->d_raw && e == cudaSuccess) e = dev_alloc(&plan->d_raw, raw_bytes);
+    if (!plan->d_pos && e == cudaSuccess) e = dev_alloc(&plan->d_pos, pos_bytes);
+    if (!plan->d_rc && e == cudaSuccess) e = dev_alloc(&plan->d_rc, ws);
+    if (!plan->d_img && e == cudaSuccess) e = dev_alloc(&plan->d_img, img_bytes);
     if (e != cudaSuccess) return cuda_status(e);
     if (!plan->copy_stream && e == cudaSuccess) e = cudaStreamCreateWithFlags(&plan->copy_stream, cudaStreamNonBlocking);
     for (cudaEvent_t &ev : plan->host_ev)

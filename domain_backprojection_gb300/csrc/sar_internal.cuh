@@ -44,6 +44,8 @@ struct RcArgs {
     const float2 *btw;       // exp(-2 pi i t / M), t in [0, M)
     const float2 *bw;        // exp(-i pi t^2 / Nr), t in [0, Nr)
     const float2 *bf;        // FFT_M of the wrapped conj(bw), divided by M
+    unsigned long long wait_limit_ns;   // bound of the staged kernels' waits (kWaitLimitNs unless the
+                                        // SAR_WAIT_LIMIT_NS knob sets another; 0 = test once)
     int max_ctas;            // CTAs of the line kernel resident on the whole device (its grid cap)
     int *err;                // device error word
 };
