@@ -271,6 +271,8 @@ def run_ours(args, rank, world, local_rank):
         out["rc_sweep"] = rc_sweep(dev, peaks, reps=max(10, min(args.steps, 50)))
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(scene, budget_s=args.cpu_seconds)
+        # the same oracle on one core, for comparison with single-thread figures
+        out["cpu_baseline_1thread"] = cpu_baseline(scene, budget_s=max(2.0, args.cpu_seconds / 3), threads=1)
     return out
 
 
