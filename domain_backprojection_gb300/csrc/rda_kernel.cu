@@ -67,33 +67,53 @@ __global__ void __launch_bounds__(N / 16, rd_min_ctas<N>()) rd_azfft_kernel(floa
     }
 }
 
-// Normalised 8-tap sinc weights for fraction f in [0, 1]: w[k] for samples r - 3 + k.  The
-// unnormalised weights (-1)^k W(f - k) prod_{j != k} (f - j) are those of the backprojection's
-// sinc option (the common factors sin(pi f) / pi and prod_j (f - j) cancel in the normalisation).
-__device__ __forceinline__ void sinc8_weights(float f, float (&w)[8])
+// Normalised 8-tap sinc weights for two fractions f.x, f.y in [0, 1] at once (float2 lanes: paired
+// FFMA2 / FMUL2 / FADD2): w[k] for samples r - 3 + k.  The unnormalised weights
+// (-1)^k W(f - k) prod_{j != k} (f - j) are those of the backprojection's sinc option (the common
+// factors sin(pi f) / pi and prod_j (f - j) cancel in the normalisation).
+__device__ __forceinline__ void sinc8_weights2(float2 f, float2 (&w)[8])
 {
     constexpr float r2 = 0.35355339059327376220f;             // sqrt(2) / 4
     constexpr float kC[8] = {r2, 0.0f, -r2, 0.5f, -r2, 0.0f, r2, -0.5f};
     constexpr float kS[8] = {r2, -0.5f, r2, 0.0f, -r2, 0.5f, -r2, 0.0f};
     constexpr float kH[8] = {-0.5f, 0.5f, -0.5f, 0.5f, -0.5f, 0.5f, -0.5f, 0.5f};
-    float sq, cq;
-    __sincosf(0.78539816339744830962f * f, &sq, &cq);
-    float d[8], pre[8];
+    float2 sq, cq;
+    __sincosf(0.78539816339744830962f * f.x, &sq.x, &cq.x);
+    __sincosf(0.78539816339744830962f * f.y, &sq.y, &cq.y);
+    float2 d[8], pre[8];
 #pragma unroll
-    for (int k = 0; k < 8; k++) d[k] = f + (float)(3 - k);
-    pre[0] = 1.0f;
+    for (int k = 0; k < 8; k++) d[k] = __fadd2_rn(f, make_float2((float)(3 - k), (float)(3 - k)));
+    pre[0] = make_float2(1.0f, 1.0f);
 #pragma unroll
-    for (int k = 1; k < 8; k++) pre[k] = pre[k - 1] * d[k - 1];
-    float suf = 1.0f, sum = 0.0f;
+    for (int k = 1; k < 8; k++) pre[k] = __fmul2_rn(pre[k - 1], d[k - 1]);
+    float2 suf = make_float2(1.0f, 1.0f), sum = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int k = 7; k >= 0; k--) {
-        w[k] = fmaf(cq, kC[k], fmaf(sq, kS[k], kH[k])) * (pre[k] * suf);
-        suf *= d[k];
-        sum += w[k];
+        const float2 wk = __ffma2_rn(cq, make_float2(kC[k], kC[k]),
+                                     __ffma2_rn(sq, make_float2(kS[k], kS[k]), make_float2(kH[k], kH[k])));
+        w[k] = __fmul2_rn(wk, __fmul2_rn(pre[k], suf));
+        suf = __fmul2_rn(suf, d[k]);
+        sum = __fadd2_rn(sum, w[k]);
     }
-    const float inv = __fdividef(1.0f, sum);
+    const float2 inv = make_float2(__fdividef(1.0f, sum.x), __fdividef(1.0f, sum.y));
 #pragma unroll
-    for (int k = 0; k < 8; k++) w[k] *= inv;
+    for (int k = 0; k < 8; k++) w[k] = __fmul2_rn(w[k], inv);
+}
+
+// One element's matched filter, conjugated for the inverse transform: v exp(+j 2 pi turns) with
+// turns = frac((2/lambda) R0) - (2/lambda)(1 - D_m) R0, the product in double-float (c = per-bin
+// coefficient (hi, lo), R0 = r_hi + r_lo).
+__device__ __forceinline__ float2 rd_filter(float2 v, float2 c, float ph0, float r_hi, float r_lo)
+{
+    const float pr = c.x * r_hi;
+    const float e = fmaf(c.x, r_lo, fmaf(c.y, r_hi, fmaf(c.x, r_hi, -pr)));
+    const float tq = (pr - rintf(pr)) + e;
+    float turns = ph0 - tq;
+    turns -= rintf(turns);
+    float sn, cs;
+    __sincosf(6.28318530717958648f * turns, &sn, &cs);
+    // conjugate of the filtered value: the inverse DFT runs as conj(DFT(conj(.)))
+    return make_float2(v.x * cs - v.y * sn, -(v.x * sn + v.y * cs));
 }
 
 // Migration correction, azimuth matched filter and azimuth IDFT of output range bin i: s [nr][N]
@@ -114,39 +134,35 @@ __global__ void __launch_bounds__(N / 16, rd_min_ctas<N>()) rd_compress_kernel(c
         const float r_hi = (float)R0, r_lo = (float)(R0 - (double)r_hi);
         const float r_bins = (float)(R0 / args.dr);                  // R0 / dr
         float2 x[16];
+        // elements in pairs (p, p + 8): the sinc weights of both come from paired float2 arithmetic
 #pragma unroll
-        for (int p = 0; p < 16; p++) {
-            const int m = t + T * p;
+        for (int p = 0; p < 8; p++) {
+            const int m0 = t + T * p, m1 = t + T * (p + 8);
             // migration: sample the range axis at q = i + (R0 / dr)(1/D_m - 1)
-            const float q = (float)i + r_bins * __ldg(args.rcm + m);
-            const float fl = floorf(q);
-            const int r0 = (int)fl - 3;
-            // the eight taps first (rows clamped into the axis, so every load is in bounds and none
-            // waits on a branch), the weights while they are in flight; taps outside the axis
-            // weigh zero
-            float2 sv[8];
-#pragma unroll
-            for (int k = 0; k < 8; k++) sv[k] = __ldg(s + (int64_t)min(max(r0 + k, 0), nr - 1) * N + m);
-            float w[8];
-            sinc8_weights(q - fl, w);
-            float2 v = make_float2(0.0f, 0.0f);
+            const float q0 = (float)i + r_bins * __ldg(args.rcm + m0);
+            const float q1 = (float)i + r_bins * __ldg(args.rcm + m1);
+            const float fl0 = floorf(q0), fl1 = floorf(q1);
+            const int r00 = (int)fl0 - 3, r01 = (int)fl1 - 3;
+            // the taps first (rows clamped into the axis, so every load is in bounds and none waits on
+            // a branch), the weights while they are in flight; taps outside the axis weigh zero
+            float2 s0[8], s1[8];
 #pragma unroll
             for (int k = 0; k < 8; k++) {
-                const float wk = (r0 + k >= 0 && r0 + k < nr) ? w[k] : 0.0f;
-                v.x = fmaf(wk, sv[k].x, v.x);
-                v.y = fmaf(wk, sv[k].y, v.y);
+                s0[k] = __ldg(s + (int64_t)min(max(r00 + k, 0), nr - 1) * N + m0);
+                s1[k] = __ldg(s + (int64_t)min(max(r01 + k, 0), nr - 1) * N + m1);
             }
-            // matched filter phase, turns: frac((2/lambda) R0) - (2/lambda)(1 - D_m) R0 (double-float)
-            const float2 c = __ldg(args.phc + m);
-            const float pr = c.x * r_hi;
-            const float e = fmaf(c.x, r_lo, fmaf(c.y, r_hi, fmaf(c.x, r_hi, -pr)));
-            float tq = (pr - rintf(pr)) + e;
-            float turns = ph0 - tq;
-            turns -= rintf(turns);
-            float sn, cs;
-            __sincosf(6.28318530717958648f * turns, &sn, &cs);
-            // conjugate of the filtered value: the inverse DFT runs as conj(DFT(conj(.)))
-            x[p] = make_float2(v.x * cs - v.y * sn, -(v.x * sn + v.y * cs));
+            float2 w[8];
+            sinc8_weights2(make_float2(q0 - fl0, q1 - fl1), w);
+            float2 v0 = make_float2(0.0f, 0.0f), v1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const float w0 = (r00 + k >= 0 && r00 + k < nr) ? w[k].x : 0.0f;
+                const float w1 = (r01 + k >= 0 && r01 + k < nr) ? w[k].y : 0.0f;
+                v0 = __ffma2_rn(make_float2(w0, w0), s0[k], v0);
+                v1 = __ffma2_rn(make_float2(w1, w1), s1[k], v1);
+            }
+            x[p] = rd_filter(v0, __ldg(args.phc + m0), ph0, r_hi, r_lo);
+            x[p + 8] = rd_filter(v1, __ldg(args.phc + m1), ph0, r_hi, r_lo);
         }
         reg_dft<N, false>(x, a, b, args.tw);
         float2 *out = img + (int64_t)i * N;
