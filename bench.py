@@ -121,9 +121,9 @@ class ClockSampler:
 
 KERNEL_SOURCES = {
     "bp_kernel": ["bp_kernel.cu", "sar_internal.cuh"],
-    "rc_reg_kernel": ["rc_kernel.cu", "sar_internal.cuh"],
-    "rc_fused_kernel": ["rc_kernel.cu", "sar_internal.cuh"],
-    "rc_mixed6000_kernel": ["rc_kernel.cu", "sar_internal.cuh"],
+    "rc_reg_kernel": ["rc_kernel.cu", "fft_reg.cuh", "sar_internal.cuh"],
+    "rc_fused_kernel": ["rc_kernel.cu", "fft_reg.cuh", "sar_internal.cuh"],
+    "rc_mixed6000_kernel": ["rc_kernel.cu", "fft_reg.cuh", "sar_internal.cuh"],
 }
 
 
