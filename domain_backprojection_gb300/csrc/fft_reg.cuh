@@ -228,7 +228,7 @@ __device__ __forceinline__ void twiddle_powers(float2 w1, float2 *w)
 // thread loads its 16/R butterflies from `src`, transforms them and writes them
 // to `dst` followed by a barrier, or keeps them in registers when kLast.  With
 // one buffer (src == dst) a barrier also separates the loads from the stores.
-template <int N, int R, int L, bool kLast, bool kOneBuf>
+template <int N, int R, int L, bool kLast, bool kOneBuf, bool kTableTw>
 __device__ __forceinline__ void reg_pass(float2 (&x)[16], const float2 *src, float2 *dst, const float2 *__restrict__ tw)
 {
     constexpr int T = N / 16, SP = N / (L * R), NB = 16 / R;
@@ -246,7 +246,15 @@ __device__ __forceinline__ void reg_pass(float2 (&x)[16], const float2 *src, flo
         const int b = t + T * i;
         const int jp = b % SP, kp = b / SP;
         float2 w[R];
-        twiddle_powers<R>(ld_twiddle(tw + SP * kp), w);
+        if constexpr (kTableTw && SP >= 8) {
+            // at most four butterfly columns kp per warp: read every power w_N^(SP kp p) from the
+            // table (SP kp p < N; the loads broadcast) instead of multiplying them out
+            w[0] = make_float2(1.0f, 0.0f);
+#pragma unroll
+            for (int p = 1; p < R; p++) w[p] = ld_twiddle(tw + SP * kp * p);
+        } else {
+            twiddle_powers<R>(ld_twiddle(tw + SP * kp), w);
+        }
 #pragma unroll
         for (int p = 1; p < R; p++) x[i * R + p] = cmul(x[i * R + p], w[p]);
         Dft<R>::run(x + i * R);
@@ -275,7 +283,7 @@ __device__ __forceinline__ void reg_pass(float2 (&x)[16], const float2 *src, flo
 // alternation from one transform to the next; `a` is the buffer the next exchange writes.  With
 // one buffer (a == b) each exchange takes a second barrier before its stores, and the transform
 // ends with one, so that the next transform may write the buffer.
-template <int N, bool kTwoBuf>
+template <int N, bool kTwoBuf, bool kTableTw = false>
 __device__ __forceinline__ void reg_dft(float2 (&x)[16], float2 *&a, float2 *&b, const float2 *__restrict__ tw)
 {
     constexpr int T = N / 16;
@@ -286,22 +294,22 @@ __device__ __forceinline__ void reg_dft(float2 (&x)[16], float2 *&a, float2 *&b,
     for (int q = 0; q < 16; q++) a[pad16(q * T + t)] = x[q];
     __syncthreads();
     if constexpr (N == 512) {
-        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
-        reg_pass<N, 2, 256, true, k1>(x, b, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
+        reg_pass<N, 2, 256, true, k1, kTableTw>(x, b, nullptr, tw);
     } else if constexpr (N == 1024) {
-        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
-        reg_pass<N, 4, 256, true, k1>(x, b, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
+        reg_pass<N, 4, 256, true, k1, kTableTw>(x, b, nullptr, tw);
     } else if constexpr (N == 2048) {
-        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
-        reg_pass<N, 8, 256, true, k1>(x, b, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
+        reg_pass<N, 8, 256, true, k1, kTableTw>(x, b, nullptr, tw);
     } else if constexpr (N == 4096) {
-        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
-        reg_pass<N, 16, 256, true, k1>(x, b, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
+        reg_pass<N, 16, 256, true, k1, kTableTw>(x, b, nullptr, tw);
     } else {
         static_assert(N == 8192, "unsupported line length");
-        reg_pass<N, 16, 16, false, k1>(x, a, b, tw);
-        reg_pass<N, 16, 256, false, k1>(x, b, a, tw);
-        reg_pass<N, 2, 4096, true, k1>(x, a, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
+        reg_pass<N, 16, 256, false, k1, kTableTw>(x, b, a, tw);
+        reg_pass<N, 2, 4096, true, k1, kTableTw>(x, a, nullptr, tw);
         float2 *c = a;                                          // three exchanges: the next one writes b
         a = b;
         b = c;
