@@ -550,8 +550,10 @@ __global__ void __launch_bounds__(200, kMulti ? kRcMixedCtas : 2) rc_mixed6000_k
 // Bluestein lines without upsampling, register-resident: the four M-point transforms of a line
 // (M = 512 .. 8192) are reg_dft passes over the thread's 16 elements t + T p (T = M / 16), the
 // line's samples in the first N positions.
+// 2 CTAs of 512 threads at M = 8192 (64 registers, a small spill): 4096 lines of 4094 samples
+// 0.4215 -> 0.3876 ms against one CTA.
 template <int M>
-constexpr int rc_blue_min_ctas() { return M >= 8192 ? 1 : M == 4096 ? 2 : (16 * 32) / (M / 16); }
+constexpr int rc_blue_min_ctas() { return M >= 8192 ? 2 : M == 4096 ? 2 : (16 * 32) / (M / 16); }
 
 template <int M>
 __global__ void __launch_bounds__(M / 16, rc_blue_min_ctas<M>())
