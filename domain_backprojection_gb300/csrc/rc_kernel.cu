@@ -15,8 +15,14 @@
 // i.e. U Nr-point inverse transforms of the same on-chip spectrum, each with a
 // per-u phase ramp (a polyphase split of the output index).
 //
-// Transforms are self-sorting mixed-radix Stockham passes (radices 16, 8, 5, 4,
-// 3, 2) between two shared-memory buffers; the spectrum stays in a third.
+// Kernels by line length Nr (launch_rc picks one):
+//   - rc_reg_kernel<N, U>1>: powers of two 512 .. 8192, register-resident radix-16
+//     transforms (fft_reg.cuh); 8192-point lines staged by bulk copy;
+//   - rc_mixed6000_kernel<U>1>: Nr = 6000, register-resident radix 10/10/10/6;
+//   - rc_fused_kernel: other even 2^a 3^b 5^c lengths, mixed-radix Stockham passes
+//     (16, 8, 5, 4, 3, 2) between two shared-memory buffers, the spectrum in a third;
+//   - rc_blue_reg_kernel<M> (U = 1) and rc_bluestein_kernel (U > 1): any other
+//     length up to 4096, as Bluestein transforms of a power-of-two length M.
 #include "fft_reg.cuh"
 
 namespace sar {
