@@ -96,6 +96,25 @@ def test_non_power_of_two_range_and_smallest_aperture():
     assert rel_l2(got, ref) <= IMG_TOL
 
 
+@pytest.mark.parametrize("na,nr", [(2048, 512), (8192, 768)])
+def test_other_aperture_lengths(na, nr):
+    # the 2048- and 8192-point azimuth transforms (one CTA per range bin of N/16 threads)
+    cfg = dataclasses.replace(synth.CONFIGS[2], n_pulses=na, prf=1200.0 * na / 1024, n_range=nr, upsample=1)
+    radar, pos = cfg.radar(), synth.track(cfg)
+    g = torch.Generator().manual_seed(na)
+    raw = torch.complex(torch.randn(na, nr, generator=g), torch.randn(na, nr, generator=g)) * 0.05
+    xyz = torch.tensor([[float(pos[na // 3, 0]), 5000.0, 0.0], [float(pos[na // 2, 0]) + 0.01, 4998.7, 0.0]],
+                       dtype=torch.float64)
+    add_echoes(raw, pos, xyz, torch.tensor([1.0, 0.7 - 0.2j], dtype=torch.complex128), radar)
+    du = cfg.velocity / cfg.prf
+    plan = sar.sar_plan_create(radar, None, 0)
+    sar.sar_plan_set_range_doppler(plan, du)
+    got = sar.sar_range_doppler(plan, raw.cuda()).cpu().numpy()
+    rc = oracle.range_compress(radar, raw.numpy(), threads=ORACLE_THREADS)
+    ref = oracle.range_doppler(radar, rc, du, threads=ORACLE_THREADS)
+    assert rel_l2(got, ref) <= IMG_TOL
+
+
 def test_range_doppler_arguments():
     radar = dataclasses.replace(synth.CONFIGS[2].radar(), upsample=1)
     plan = sar.sar_plan_create(radar, None, 0)
