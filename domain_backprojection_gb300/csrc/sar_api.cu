@@ -3,6 +3,8 @@
 // range compression, backprojection and image formation entry points.
 #include <algorithm>
 #include <cmath>
+#include <cstdarg>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -70,6 +72,23 @@ struct DeviceGuard {
 
 bool finite_pos(double v) { return std::isfinite(v) && v > 0.0; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Optional trace on stderr (SAR_LOG=1 in the environment when the library first logs): plan
+// parameters and the kernels chosen, device-side flags.  Silent otherwise.
+void sar_log(const char *fmt, ...)
+{
+    static const int on = [] {
+        const char *v = std::getenv("SAR_LOG");
+        return v && v[0] == '1' ? 1 : 0;
+    }();
+    if (!on) return;
+    va_list ap;
+    va_start(ap, fmt);
+    std::fputs("[sar] ", stderr);
+    std::vfprintf(stderr, fmt, ap);
+    std::fputc('\n', stderr);
+    va_end(ap);
+}
 
 // Fault-injection hook for tests: with SAR_INJECT_ALLOC_FAILURE=1 in the environment every device
 // allocation the library makes reports cudaErrorMemoryAllocation without calling CUDA, so the
@@ -579,6 +598,15 @@ sar_status sar_plan_create(const sar_radar *radar, const sar_grid *grid, int dev
         free_plan(p);
         return st;
     }
+    sar_log("plan %p: device %d, Na %d, Nr %d (%s), U %d, fc %.6g Hz, B %.6g Hz, Tp %.6g s, fs %.6g Hz, "
+            "range_start %.6f m", (void *)p, device, radar->n_pulses, radar->n_range,
+            p->rc.bm ? "Bluestein" : "mixed radix", radar->upsample, radar->fc, radar->bandwidth, radar->pulse_width,
+            radar->fs, radar->range_start);
+    if (p->has_grid)
+        sar_log("plan %p: grid %d x %d at (%.3f, %.3f) m, tiles %d x %d of %d x %d pixels, window %d entries, "
+                "%d resident backprojection CTAs, up to %d pulse slices", (void *)p, p->grid.nx, p->grid.ny,
+                p->grid.dx, p->grid.dy, p->bp.tiles_x, p->bp.tiles_y, p->bp.tile_w, p->bp.tile_h, p->bp.w,
+                p->bp_slots, p->bp_max_slices);
     *out = p;
     return SAR_OK;
 }
@@ -819,6 +847,7 @@ sar_status sar_plan_sync(sar_plan plan, void *stream)
         e = cudaMemset(plan->d_err, 0, sizeof(int));
         if (e != cudaSuccess) return SAR_ERR_CUDA;
     }
+    if (flags) sar_log("plan %p: device flags 0x%x", (void *)plan, flags);
     if (flags & sar::kDevErrBounds) return SAR_ERR_INTERNAL;
     if (flags & sar::kDevErrTimeout) return SAR_ERR_TIMEOUT;
     if (flags & sar::kDevErrGeometry) return SAR_ERR_UNSUPPORTED;

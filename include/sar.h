@@ -13,7 +13,9 @@
  *    except where stated.  Argument errors are detected before anything is
  *    launched.  Device-side error flags (bounds checks, geometry validity)
  *    are reported by sar_plan_sync.
- *  - Errors are return codes only; nothing aborts, traps or throws.
+ *  - Errors are return codes only; nothing aborts, traps or throws.  The
+ *    library prints nothing, except a trace of plan parameters, kernel
+ *    choices and device flags on stderr when SAR_LOG=1 is in the environment.
  *  - A plan may be used from one host thread at a time.  Calls on different
  *    streams that share one plan are serialised by the caller.
  *

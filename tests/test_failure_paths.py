@@ -74,3 +74,21 @@ def test_injected_allocation_failures(monkeypatch):
     sar.sar_plan_sync(plan)
     assert np.abs(out.numpy() - ref.cpu().numpy()).max() <= 1e-5 * np.abs(ref.cpu().numpy()).max()
     sar.sar_plan_set_range_doppler(rd_plan, 0.1)
+
+
+def test_log_trace_on_request():
+    # SAR_LOG=1: plan parameters and kernel choices go to stderr (a fresh process: the switch is read
+    # once); without it the library prints nothing
+    import os
+    import subprocess
+    import sys
+    code = ("import synth, domain_backprojection_gb300 as sar; c = synth.CONFIGS[1]; "
+            "p = sar.sar_plan_create(c.radar(), c.grid(), 0)")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, SAR_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert "[sar] plan" in r.stderr and "tiles" in r.stderr
+    env.pop("SAR_LOG")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "[sar]" not in r.stderr
