@@ -115,6 +115,35 @@ def test_other_aperture_lengths(na, nr):
     assert rel_l2(got, ref) <= IMG_TOL
 
 
+def test_range_doppler_captures_into_a_cuda_graph():
+    # sar_range_doppler enqueues its launches with no allocation or synchronisation once the plan's
+    # tables exist: capture it once, replay it on new echoes copied into the captured buffer
+    cfg = dataclasses.replace(synth.CONFIGS[2], n_pulses=512, prf=600.0, n_range=1024, upsample=1)
+    radar = cfg.radar()
+    plan = sar.sar_plan_create(radar, None, 0)
+    sar.sar_plan_set_range_doppler(plan, cfg.velocity / cfg.prf)
+    raw = torch.zeros(512, 1024, dtype=torch.complex64, device="cuda")
+    ws = torch.empty(sar.sar_range_doppler_workspace_size(plan), dtype=torch.uint8, device="cuda")
+    img = torch.empty(1024, 512, dtype=torch.complex64, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        sar.sar_range_doppler(plan, raw, img, ws)                    # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sar.sar_range_doppler(plan, raw, img, ws)
+    for seed in (1, 2):
+        gen = torch.Generator().manual_seed(seed)
+        new = torch.complex(torch.randn(512, 1024, generator=gen), torch.randn(512, 1024, generator=gen)).cuda()
+        raw.copy_(new)
+        g.replay()
+        want = sar.sar_range_doppler(plan, new)
+        torch.cuda.synchronize()
+        assert torch.equal(img, want)
+    sar.sar_plan_sync(plan)
+
+
 def test_range_doppler_arguments():
     radar = dataclasses.replace(synth.CONFIGS[2].radar(), upsample=1)
     plan = sar.sar_plan_create(radar, None, 0)
