@@ -269,6 +269,8 @@ def run_ours(args, rank, world, local_rank):
         out["bp_variants"] = bp_variants(scene, dev, reps=max(5, min(args.steps, 20)))
     if not args.no_rc_sweep:
         out["rc_sweep"] = rc_sweep(dev, peaks, reps=max(10, min(args.steps, 50)))
+    if not args.no_scenes:
+        out["scenes"] = other_scenes(dev, peaks, fp32_peak, reps=max(5, min(args.steps, 20)))
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(scene, budget_s=args.cpu_seconds)
         # the same oracle on one core, for comparison with single-thread figures
@@ -422,6 +424,64 @@ def rda_bench(scene, dev, peaks, reps=10):
             "launches": 4, "pages_context": "Apple M1, 4096x4096 range-Doppler: 370 ms (other hardware)"}
 
 
+def other_scenes(dev, peaks, fp32_peak, reps=20):
+    """The other backprojection scenes, each formed as the headline step forms its image (range
+    compression into polyphase planes, then backprojection): the tiny (256 x 1024, 128^2), small
+    (1024 x 2048, 512^2) and large curved-track (16384 x 8192, 2048^2, seeded motion errors)
+    scenes.  Per scene: step time, pixel-pulse and line rates, the backprojection kernel's fraction of
+    the FP32 peak and the range compression's fraction of the measured HBM bandwidth.  The tiny and
+    small scenes' inputs fit in L2, so their rates are L2-warm; the large scene's do not."""
+    import torch
+    import domain_backprojection_gb300 as sar
+    import synth
+
+    res = {}
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    for cid in (1, 2, 4):
+        cfg = synth.CONFIGS[cid]
+        scene = synth.make_scene(cid, device=dev)
+        radar, grid = scene["radar"], scene["grid"]
+        plan = sar.sar_plan_create(radar, grid, dev.index)
+        sar.sar_plan_set_rc_layout(plan, sar.SAR_RC_POLYPHASE)
+        rc = torch.empty(cfg.n_pulses, radar.n_range * radar.upsample, dtype=torch.complex64, device=dev)
+        img = torch.empty(grid.ny, grid.nx, dtype=torch.complex64, device=dev)
+        n = reps if cid != 4 else max(3, reps // 4)
+        for _ in range(3):
+            sar.sar_range_compress(plan, scene["raw"], rc)
+            sar.sar_backproject(plan, rc, scene["pos"], image=img)
+        sar.sar_plan_sync(plan)
+        sar.sar_plan_set_timing(plan, True)
+        sar.sar_plan_kernel_times(plan)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            sar.sar_range_compress(plan, scene["raw"], rc)
+            sar.sar_backproject(plan, rc, scene["pos"], image=img)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        sar.sar_plan_sync(plan)
+        kt = sar.sar_plan_kernel_times(plan)
+        step_ms = e0.elapsed_time(e1) / n
+        bp_ms = kt["bp_ms"] / kt["bp_calls"]
+        rc_ms = kt["rc_ms"] / kt["rc_calls"]
+        pp = cfg.pixel_pulses
+        rc_gbs = cfg.n_pulses * 8 * radar.n_range * (1 + radar.upsample) / (rc_ms * 1e-3) / 1e9
+        bp_tflops = FLOPS_PER_PIXEL_PULSE * pp / (bp_ms * 1e-3) / 1e12
+        res[str(cid)] = {
+            "workload": f"Na={cfg.n_pulses} Nr={radar.n_range} U={radar.upsample} image {grid.nx}x{grid.ny} @ {grid.dx} m"
+                        + (", curved track" if cid == 4 else ""),
+            "pixel_pulses": pp, "step_ms": round(step_ms, 4),
+            "step_gpix_pulse_per_s": round(pp / (step_ms * 1e-3) / 1e9, 1),
+            "bp_kernel_ms": round(bp_ms, 4), "bp_gpix_pulse_per_s": round(pp / (bp_ms * 1e-3) / 1e9, 1),
+            "bp_frac_fp32": round(bp_tflops / fp32_peak, 4),
+            "rc_kernel": rc_kernel_name(radar.n_range, radar.upsample), "rc_kernel_ms": round(rc_ms, 4),
+            "rc_lines_per_s": round(cfg.n_pulses / (rc_ms * 1e-3), 1), "rc_frac_hbm": round(rc_gbs / hbm, 4),
+            "l2": "inputs fit in L2" if cid != 4 else "inputs 1.07 GB raw, 8.6 GB compressed lines"}
+        del plan, rc, img, scene
+        torch.cuda.empty_cache()
+    return res
+
+
 def rc_sweep(dev, peaks, reps=20, n_sets=4):
     """Range compression alone on the range-only workload: 4096 lines of Nr in {4096, 8192, 6000}
     samples, U = 1, four rotating input sets; lines/s and fraction of the measured HBM bandwidth."""
@@ -530,6 +590,7 @@ def main():
     ap.add_argument("--no-rc-sweep", action="store_true")
     ap.add_argument("--no-bp-variants", action="store_true")
     ap.add_argument("--no-rda", action="store_true")
+    ap.add_argument("--no-scenes", action="store_true")
     ap.add_argument("--profile-case", nargs="?", const="spotlight", default=None,
                     help="run a short untimed case for profiler captures and exit: 'spotlight' (default) forms two "
                          "images of the spotlight scene (RC then BP, polyphase planes); 'sweepNR' (e.g. NR = 4096, 8192, "
