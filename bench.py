@@ -325,9 +325,10 @@ def profile_case(case="spotlight"):
         sar.sar_plan_sync(plan)
         print(json.dumps({"profile_case": "ok", "workload": "range-Doppler, 4096 x 4096, spotlight scene raw echoes"}))
         return
-    if case != "spotlight":
+    scene_ids = {"spotlight": CONFIG_ID, "scene1": 1, "scene2": 2, "scene4": 4}
+    if case not in scene_ids:
         raise SystemExit(f"unknown profile case {case!r}")
-    scene = synth.make_scene(CONFIG_ID, device="cuda")
+    scene = synth.make_scene(scene_ids[case], device="cuda")
     radar = scene["radar"]
     plan = sar.sar_plan_create(radar, scene["grid"], 0)
     sar.sar_plan_set_rc_layout(plan, sar.SAR_RC_POLYPHASE)
@@ -336,7 +337,9 @@ def profile_case(case="spotlight"):
         sar.sar_range_compress(plan, scene["raw"], rc)
         sar.sar_backproject(plan, rc, scene["pos"])
     sar.sar_plan_sync(plan)
-    print(json.dumps({"profile_case": "ok", "workload": "spotlight 4096x4096 U=8, 1024x1024 image"}))
+    g = scene["grid"]
+    print(json.dumps({"profile_case": "ok", "workload": f"{case}: Na={radar.n_pulses} Nr={radar.n_range} "
+                                                        f"U={radar.upsample}, {g.nx}x{g.ny} image"}))
 
 
 def bp_variants(scene, dev, reps=10):
@@ -593,7 +596,8 @@ def main():
     ap.add_argument("--no-scenes", action="store_true")
     ap.add_argument("--profile-case", nargs="?", const="spotlight", default=None,
                     help="run a short untimed case for profiler captures and exit: 'spotlight' (default) forms two "
-                         "images of the spotlight scene (RC then BP, polyphase planes); 'sweepNR' (e.g. NR = 4096, 8192, "
+                         "images of the spotlight scene (RC then BP, polyphase planes), 'scene1', 'scene2' and 'scene4' "
+                         "the same on the tiny, small and large curved-track scenes; 'sweepNR' (e.g. NR = 4096, 8192, "
                          "6000, 4094) range-compresses the 4096 lines of the range-only workload three times; 'rda' forms "
                          "two range-Doppler images of the spotlight scene's raw echoes")
     args = ap.parse_args()

@@ -3,12 +3,13 @@
 // the linearly interpolated range-compressed echo at its range, multiplied by
 // exp(+j 4 pi fc R / c0).
 //
-// Work decomposition.  One CTA owns a 64 x 32 pixel tile, long in azimuth (x):
-// pixels that differ only in x lie at nearly the same range, so the window of
-// compressed samples a tile touches grows with its range (y) extent only and
-// staging it is shared by twice as many pixels.  Warps run along x, so the 32
-// lanes of a warp read nearly the same samples; each thread keeps four pixels'
-// complex sums in registers for the whole pulse range.  The CTA walks the
+// Work decomposition.  One CTA owns a tile of 2048 pixels, long in azimuth (x): 128 x 16, 64 x 32
+// or 32 x 64 pixels, the longest whose half-diagonal stays within the range-series bound (the plan
+// picks it).  Pixels that differ only in x lie at nearly the same range, so the window of
+// compressed samples a tile touches grows with its range (y) extent only and staging it is shared
+// by more pixels.  Warps run along x, so the 32 lanes of a warp read nearly the same samples; each
+// thread keeps eight pixels' complex sums (one column, eight consecutive rows) in registers for
+// the whole pulse range.  The CTA walks the
 // pulses in batches: for each pulse of a batch it first evaluates, in float64,
 // the range R0 from the antenna to the tile centre, then stages the window of
 // compressed samples the tile can touch in shared memory (section 2.3 of the
@@ -23,8 +24,8 @@
 // from the tile centre, w the antenna-to-centre vector and g = 2 w.d/R0 + |d|^2/R0,
 //     R - R0 = g/2 - g^2/(8 R0) + g^3/(16 R0^2) - 5 g^4/(128 R0^3) + O(g^5/R0^4),
 // evaluated by Horner's rule in range-bin units (the binomial series of
-// R0 sqrt(1 + g/R0)).  |d| <= 11 m and R0 >= 100 tile half-diagonals keep the
-// truncation below 1e-7 m.
+// R0 sqrt(1 + g/R0)).  |d| <= h (the tile half-diagonal, at most 32 m) and R0 >= 100 h
+// keep the truncation below 9e-9 h, 3e-7 m (below 1e-9 m for 16 m tiles at 5.8 km).
 //
 // Interpolation and phase in one staged pair.  With q the pixel's fractional
 // bin relative to the window origin o (half a bin shifted: qm = q - 1/2) and

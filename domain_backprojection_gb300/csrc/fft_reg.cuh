@@ -25,12 +25,21 @@ __device__ __forceinline__ float2 cmul(float2 a, float2 b)
 }
 __device__ __forceinline__ float2 cconj(float2 a) { return make_float2(a.x, -a.y); }
 __device__ __forceinline__ float2 mul_minus_i(float2 a) { return make_float2(a.y, -a.x); }   // -i a
+__device__ __forceinline__ float2 mul_plus_i(float2 a) { return make_float2(-a.y, a.x); }    // +i a
+// -i a for a forward DFT, +i a for an inverse one
+template <bool kInv>
+__device__ __forceinline__ float2 mul_mi(float2 a) { return kInv ? mul_plus_i(a) : mul_minus_i(a); }
+// a times w for a forward DFT, a times conj(w) for an inverse one
+template <bool kInv>
+__device__ __forceinline__ float2 cmul_c(float2 a, float wr, float wi) { return cmul(a, make_float2(wr, kInv ? -wi : wi)); }
 __device__ __forceinline__ float2 cscale(float2 a, float s) { return make_float2(a.x * s, a.y * s); }
 
-// Forward DFTs of small sizes, in registers: y_k = sum_j a_j exp(-2 pi i j k / R).
-template <int R> struct Dft;
+// DFTs of small sizes, in registers: y_k = sum_j a_j exp(-2 pi i j k / R) (forward), or with
+// exp(+2 pi i j k / R) for kInv (radices 2, 4, 8 and 16; every constant conjugated, so that the
+// inverse of a equals conj(forward(conj(a))) bit for bit).
+template <int R, bool kInv = false> struct Dft;
 
-template <> struct Dft<2> {
+template <bool kInv> struct Dft<2, kInv> {
     static __device__ __forceinline__ void run(float2 *a)
     {
         float2 t = a[0];
@@ -39,7 +48,7 @@ template <> struct Dft<2> {
     }
 };
 
-template <> struct Dft<3> {
+template <> struct Dft<3, false> {
     static __device__ __forceinline__ void run(float2 *a)
     {
         const float s = 0.86602540378443864676f;   // sin(2 pi / 3)
@@ -53,11 +62,11 @@ template <> struct Dft<3> {
     }
 };
 
-template <> struct Dft<4> {
+template <bool kInv> struct Dft<4, kInv> {
     static __device__ __forceinline__ void run(float2 *a)
     {
         float2 s02 = cadd(a[0], a[2]), d02 = csub(a[0], a[2]);
-        float2 s13 = cadd(a[1], a[3]), d13 = mul_minus_i(csub(a[1], a[3]));
+        float2 s13 = cadd(a[1], a[3]), d13 = mul_mi<kInv>(csub(a[1], a[3]));
         a[0] = cadd(s02, s13);
         a[2] = csub(s02, s13);
         a[1] = cadd(d02, d13);
@@ -65,7 +74,7 @@ template <> struct Dft<4> {
     }
 };
 
-template <> struct Dft<5> {
+template <> struct Dft<5, false> {
     static __device__ __forceinline__ void run(float2 *a)
     {
         const float c1 = 0.30901699437494742410f;    // cos(2 pi / 5)
@@ -90,7 +99,7 @@ template <> struct Dft<5> {
 
 // 6 = 2 x 3 and 10 = 2 x 5: DFTs of the even and the odd samples, the odd ones turned by
 // exp(-2 pi i k / R), then sums and differences.
-template <> struct Dft<6> {
+template <> struct Dft<6, false> {
     static __device__ __forceinline__ void run(float2 *a)
     {
         const float h = 0.86602540378443864676f;    // sin(2 pi / 6)
@@ -108,7 +117,7 @@ template <> struct Dft<6> {
     }
 };
 
-template <> struct Dft<10> {
+template <> struct Dft<10, false> {
     static __device__ __forceinline__ void run(float2 *a)
     {
         const float c1 = 0.80901699437494742410f, s1 = 0.58778525229247312917f;   // 2 pi / 10
@@ -129,18 +138,23 @@ template <> struct Dft<10> {
     }
 };
 
-template <> struct Dft<8> {
+template <bool kInv> struct Dft<8, kInv> {
     static __device__ __forceinline__ void run(float2 *a)
     {
         const float r = 0.70710678118654752440f;
         float2 e[4] = {a[0], a[2], a[4], a[6]};
         float2 o[4] = {a[1], a[3], a[5], a[7]};
-        Dft<4>::run(e);
-        Dft<4>::run(o);
-        // o_k *= exp(-2 pi i k / 8)
-        o[1] = make_float2(r * (o[1].x + o[1].y), r * (o[1].y - o[1].x));
-        o[2] = mul_minus_i(o[2]);
-        o[3] = make_float2(r * (o[3].y - o[3].x), -r * (o[3].x + o[3].y));
+        Dft<4, kInv>::run(e);
+        Dft<4, kInv>::run(o);
+        // o_k *= exp(-2 pi i k / 8), or exp(+2 pi i k / 8)
+        if constexpr (kInv) {
+            o[1] = make_float2(r * (o[1].x - o[1].y), r * (o[1].y + o[1].x));
+            o[3] = make_float2(-r * (o[3].x + o[3].y), r * (o[3].x - o[3].y));
+        } else {
+            o[1] = make_float2(r * (o[1].x + o[1].y), r * (o[1].y - o[1].x));
+            o[3] = make_float2(r * (o[3].y - o[3].x), -r * (o[3].x + o[3].y));
+        }
+        o[2] = mul_mi<kInv>(o[2]);
 #pragma unroll
         for (int k = 0; k < 4; k++) {
             a[k] = cadd(e[k], o[k]);
@@ -149,7 +163,7 @@ template <> struct Dft<8> {
     }
 };
 
-template <> struct Dft<16> {
+template <bool kInv> struct Dft<16, kInv> {
     static __device__ __forceinline__ void run(float2 *a)
     {
         // n = 4 n1 + n2, k = k1 + 4 k2: inner DFT4 over n1, twiddle w16^(n2 k1), outer DFT4 over n2
@@ -157,25 +171,25 @@ template <> struct Dft<16> {
 #pragma unroll
         for (int n2 = 0; n2 < 4; n2++) {
             float2 t[4] = {a[n2], a[4 + n2], a[8 + n2], a[12 + n2]};
-            Dft<4>::run(t);
+            Dft<4, kInv>::run(t);
 #pragma unroll
             for (int k1 = 0; k1 < 4; k1++) b[n2][k1] = t[k1];
         }
         const float c = 0.92387953251128675613f, s = 0.38268343236508977173f, r = 0.70710678118654752440f;
-        // w16^m = exp(-2 pi i m / 16) for m = n2 * k1
-        b[1][1] = cmul(b[1][1], make_float2(c, -s));
-        b[1][2] = cmul(b[1][2], make_float2(r, -r));
-        b[1][3] = cmul(b[1][3], make_float2(s, -c));
-        b[2][1] = cmul(b[2][1], make_float2(r, -r));
-        b[2][2] = mul_minus_i(b[2][2]);
-        b[2][3] = cmul(b[2][3], make_float2(-r, -r));
-        b[3][1] = cmul(b[3][1], make_float2(s, -c));
-        b[3][2] = cmul(b[3][2], make_float2(-r, -r));
-        b[3][3] = cmul(b[3][3], make_float2(-c, s));
+        // w16^m = exp(-2 pi i m / 16) for m = n2 * k1 (conjugated for the inverse)
+        b[1][1] = cmul_c<kInv>(b[1][1], c, -s);
+        b[1][2] = cmul_c<kInv>(b[1][2], r, -r);
+        b[1][3] = cmul_c<kInv>(b[1][3], s, -c);
+        b[2][1] = cmul_c<kInv>(b[2][1], r, -r);
+        b[2][2] = mul_mi<kInv>(b[2][2]);
+        b[2][3] = cmul_c<kInv>(b[2][3], -r, -r);
+        b[3][1] = cmul_c<kInv>(b[3][1], s, -c);
+        b[3][2] = cmul_c<kInv>(b[3][2], -r, -r);
+        b[3][3] = cmul_c<kInv>(b[3][3], -c, s);
 #pragma unroll
         for (int k1 = 0; k1 < 4; k1++) {
             float2 t[4] = {b[0][k1], b[1][k1], b[2][k1], b[3][k1]};
-            Dft<4>::run(t);
+            Dft<4, kInv>::run(t);
 #pragma unroll
             for (int k2 = 0; k2 < 4; k2++) a[k1 + 4 * k2] = t[k2];
         }
@@ -233,8 +247,9 @@ __device__ __forceinline__ void twiddle_powers(float2 w1, float2 *w)
 // One pass of radix R after L elements have been combined (L > 1): every
 // thread loads its 16/R butterflies from `src`, transforms them and writes them
 // to `dst` followed by a barrier, or keeps them in registers when kLast.  With
-// one buffer (src == dst) a barrier also separates the loads from the stores.
-template <int N, int R, int L, bool kLast, bool kOneBuf, bool kTableTw>
+// one buffer (src == dst) a barrier also separates the loads from the stores.  An inverse pass
+// (kInv) takes its twiddles from the conjugated table.
+template <int N, int R, int L, bool kLast, bool kOneBuf, bool kTableTw, bool kInv = false>
 __device__ __forceinline__ void reg_pass(float2 (&x)[16], const float2 *src, float2 *dst, const float2 *__restrict__ tw)
 {
     constexpr int T = N / 16, SP = N / (L * R), NB = 16 / R;
@@ -263,7 +278,7 @@ __device__ __forceinline__ void reg_pass(float2 (&x)[16], const float2 *src, flo
         }
 #pragma unroll
         for (int p = 1; p < R; p++) x[i * R + p] = cmul(x[i * R + p], w[p]);
-        Dft<R>::run(x + i * R);
+        Dft<R, kInv>::run(x + i * R);
         if (!kLast) {
 #pragma unroll
             for (int q = 0; q < R; q++) dst[pad16((kp + L * q) * SP + jp)] = x[i * R + q];
@@ -282,40 +297,42 @@ __device__ __forceinline__ void reg_pass(float2 (&x)[16], const float2 *src, flo
     }
 }
 
-// Forward DFT of the line held as x[p] = element t + T p; result in the same layout.
+// Forward DFT of the line held as x[p] = element t + T p; result in the same layout.  With kInv
+// the unnormalised inverse DFT instead, given the conjugated twiddle table: conjugated constants
+// throughout, bit-identical to conjugating the input and the output of the forward transform.
 // With two buffers (kTwoBuf) the exchanges alternate between them, so that each needs one
 // barrier: every write goes to the buffer read two exchanges earlier, and the barrier of the
 // exchange in between orders all of those reads before it.  The pair (a, b) carries the
 // alternation from one transform to the next; `a` is the buffer the next exchange writes.  With
 // one buffer (a == b) each exchange takes a second barrier before its stores, and the transform
 // ends with one, so that the next transform may write the buffer.
-template <int N, bool kTwoBuf, bool kTableTw = false>
+template <int N, bool kTwoBuf, bool kTableTw = false, bool kInv = false>
 __device__ __forceinline__ void reg_dft(float2 (&x)[16], float2 *&a, float2 *&b, const float2 *__restrict__ tw)
 {
     constexpr int T = N / 16;
     constexpr bool k1 = !kTwoBuf;
     const int t = threadIdx.x;
-    Dft<16>::run(x);                                            // pass 1: L = 1, no twiddles
+    Dft<16, kInv>::run(x);                                      // pass 1: L = 1, no twiddles
 #pragma unroll
     for (int q = 0; q < 16; q++) a[pad16(q * T + t)] = x[q];
     __syncthreads();
     if constexpr (N == 512) {
-        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
-        reg_pass<N, 2, 256, true, k1, kTableTw>(x, b, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw, kInv>(x, a, b, tw);
+        reg_pass<N, 2, 256, true, k1, kTableTw, kInv>(x, b, nullptr, tw);
     } else if constexpr (N == 1024) {
-        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
-        reg_pass<N, 4, 256, true, k1, kTableTw>(x, b, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw, kInv>(x, a, b, tw);
+        reg_pass<N, 4, 256, true, k1, kTableTw, kInv>(x, b, nullptr, tw);
     } else if constexpr (N == 2048) {
-        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
-        reg_pass<N, 8, 256, true, k1, kTableTw>(x, b, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw, kInv>(x, a, b, tw);
+        reg_pass<N, 8, 256, true, k1, kTableTw, kInv>(x, b, nullptr, tw);
     } else if constexpr (N == 4096) {
-        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
-        reg_pass<N, 16, 256, true, k1, kTableTw>(x, b, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw, kInv>(x, a, b, tw);
+        reg_pass<N, 16, 256, true, k1, kTableTw, kInv>(x, b, nullptr, tw);
     } else {
         static_assert(N == 8192, "unsupported line length");
-        reg_pass<N, 16, 16, false, k1, kTableTw>(x, a, b, tw);
-        reg_pass<N, 16, 256, false, k1, kTableTw>(x, b, a, tw);
-        reg_pass<N, 2, 4096, true, k1, kTableTw>(x, a, nullptr, tw);
+        reg_pass<N, 16, 16, false, k1, kTableTw, kInv>(x, a, b, tw);
+        reg_pass<N, 16, 256, false, k1, kTableTw, kInv>(x, b, a, tw);
+        reg_pass<N, 2, 4096, true, k1, kTableTw, kInv>(x, a, nullptr, tw);
         float2 *c = a;                                          // three exchanges: the next one writes b
         a = b;
         b = c;

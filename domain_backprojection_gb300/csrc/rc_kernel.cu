@@ -292,17 +292,17 @@ __device__ __forceinline__ void rc_reg_line(float2 (&x)[16], float2 *&a, float2 
 #pragma unroll
         for (int p = 0; p < 16; p++) y[p] = cmul(x[p], __ldg(args.h + t + T * p));
         for (int u = 0; u < U; u++) {
-            // y = Y exp(+j 2 pi k_s u / (U N)); inverse transform by the conjugate identity
+            // y = Y exp(+j 2 pi k_s u / (U N)), then its inverse transform (conjugated twiddles)
 #pragma unroll
-            for (int p = 0; p < 16; p++) x[p] = cconj(y[p]);
-            reg_dft<N, rc_reg_two_buffers<N, kMulti>(), (N < 8192)>(x, a, b, args.tw);
+            for (int p = 0; p < 16; p++) x[p] = y[p];
+            reg_dft<N, rc_reg_two_buffers<N, kMulti>(), (N < 8192), true>(x, a, b, args.twi);
             if (args.planar) {
                 float2 *plane = out + (int64_t)u * N;
 #pragma unroll
-                for (int p = 0; p < 16; p++) plane[t + T * p] = cconj(x[p]);
+                for (int p = 0; p < 16; p++) plane[t + T * p] = x[p];
             } else {
 #pragma unroll
-                for (int p = 0; p < 16; p++) out[(int64_t)U * (t + T * p) + u] = cconj(x[p]);
+                for (int p = 0; p < 16; p++) out[(int64_t)U * (t + T * p) + u] = x[p];
             }
             if (u + 1 < U) {
 #pragma unroll

@@ -36,6 +36,7 @@ struct RcArgs {
     const float2 *ptw_hi;    // exp(-2 pi i (hi << bits) / (U Nr))
     const float2 *ptw_lo;    // exp(-2 pi i lo / (U Nr)), lo < 2^bits
     const float2 *ramp;      // exp(+2 pi i k_s / (U Nr)) for k in [0, Nr), k_s the signed frequency
+    const float2 *twi;       // conj(w_N^t): the inverse transforms' twiddles
     int planar;              // output layout: 0 natural (sample U m + u at U m + u), 1 planes (at u Nr + m)
     // Bluestein transforms (lengths other than 2^a 3^b 5^c, or odd): bm = 0 when unused
     int bm;                  // convolution length M (a power of two >= 2 Nr - 1)
