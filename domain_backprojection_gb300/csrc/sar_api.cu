@@ -407,7 +407,7 @@ sar_status setup_bp(sar_plan p)
     // 216 KB of shared memory per SM, split between the resident CTAs: 48 pulses' parameters, the
     // rest for raw and staged rows; the kernel sizes its rows from the windows it actually stages
     const int pulses_per_batch = 48;
-    const int stage_bytes = 216 * 1024 / sar::kBpCtasPerSm - 15 * pulses_per_batch * (int)sizeof(float4);
+    const int stage_bytes = 216 * 1024 / sar::kBpCtasPerSm - sar::kBpParamSlots * pulses_per_batch * (int)sizeof(float4);
     a.tile_w = 32;
     for (int tw : {128, 64}) {
         const int th = sar::kBpThreads * sar::kBpRowsPerThread / tw;

@@ -82,6 +82,7 @@ constexpr int kBpRowsPerThread = 8;   // pixel rows each thread accumulates
 constexpr int kBpThreads = 256;        // threads per CTA: a tile of kBpThreads * kBpRowsPerThread pixels,
                                        // 128 x 16, 64 x 32 or 32 x 64 (x along azimuth), chosen per plan
 constexpr int kBpCtasPerSm = 3;        // resident CTAs per SM the kernel is built for (registers, shared memory)
+constexpr int kBpParamSlots = 9;       // float4 slots of shared memory per batch pulse: 3 batches x (2 parameters + window)
 constexpr int kBpMaxSlices = 32;
 
 // Backprojection variants (one at a time; a plan selects one with its option setters).
