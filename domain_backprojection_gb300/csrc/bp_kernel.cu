@@ -442,6 +442,10 @@ __device__ __forceinline__ void cp_async8(unsigned dst, const void *src, int src
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+__device__ __forceinline__ void cp_async16(unsigned dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
@@ -529,9 +533,9 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
     float2 *raw = reinterpret_cast<float2 *>(dyn);                           // [pb_max][rw]
     char *stage = reinterpret_cast<char *>(dyn) + (size_t)pb_max * rw * 8;   // [pb_max][row_n] entries
 
-    // entry e of pulse row p lives at stage + p row_n + e - e_lo(p) + kTapsBefore; win.w holds
-    // p row_n - e_lo(p) + kTapsBefore, and the address of entry round(qm) + wh is formed from the bit
-    // pattern of qm + magic with 32-bit wrap-around
+    // entry e of pulse row p lives at stage + p row_n + e - e_lo(p) + kTapsBefore (e_lo = win.y), and
+    // the address of entry round(qm) + wh is formed from the bit pattern of qm + magic with 32-bit
+    // wrap-around
     const unsigned stage_row0 = (unsigned)__cvta_generic_to_shared(stage) + kEb * (unsigned)wh - kEb * kRoundMagicBits;
     const unsigned raw_base = (unsigned)__cvta_generic_to_shared(raw);
 
@@ -593,12 +597,12 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
             }
         }
     };
-    // one pulse's table entry -> its slot of the pair quads and its window
+    // one pulse's table entry -> its two parameter slots and its window (the entry's words as they
+    // are: the window's integers travel as float bit patterns)
     auto put_params = [&](int p, const float4 pa, const float4 pc, const float4 wf, float4 *quad, int4 *win) {
         quad[2 * p] = pa;
         quad[2 * p + 1] = pc;
-        const int e_lo = __float_as_int(wf.y);
-        win[p] = make_int4(__float_as_int(wf.x), e_lo, __float_as_int(wf.z), p * row_n - e_lo + kTapsBefore);
+        win[p] = make_int4(__float_as_int(wf.x), __float_as_int(wf.y), __float_as_int(wf.z), __float_as_int(wf.w));
     };
     auto load_params = [&](int n, int count, float4 *quad, int4 *win) {
         if ((int)threadIdx.x < count) {
@@ -628,19 +632,21 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
         const int pb2 = max(0, min(pb_max, p_end - n2));
         // the next batch's samples, copied while this batch is computed
         if (pb1 > 0) issue_raw(n1, pb1, wins + pb_cap * buf1);
-        // the batch after next: parameters into registers now, into shared memory after the loop
-        float4 nx0, nx1, nx2;
+        // the batch after next: its table entries copied into their slots while this batch is
+        // computed (no registers held across the pixel loop)
         if ((int)threadIdx.x < pb2) {
             const float4 *src = tab + 3 * (int64_t)(n2 + threadIdx.x);
-            nx0 = __ldg(src);
-            nx1 = __ldg(src + 1);
-            nx2 = __ldg(src + 2);
+            const unsigned q = (unsigned)__cvta_generic_to_shared(quads + 2 * pb_cap * buf2 + 2 * threadIdx.x);
+            cp_async16(q, src);
+            cp_async16(q + 16u, src + 1);
+            cp_async16((unsigned)__cvta_generic_to_shared(wins + pb_cap * buf2 + threadIdx.x), src + 2);
         }
+        cp_async_commit();
         // ---- pixel x pulse inner loop
 #pragma unroll 2
         for (int p = 0; p < pb; p++) {
             const int4 wv = win[p];
-            const unsigned base = stage_row0 + (unsigned)wv.w * kEb;
+            const unsigned base = stage_row0 + (unsigned)(p * row_n - wv.y + kTapsBefore) * kEb;
             if constexpr (kSinc) pixel_pulse_sinc<kCheck>(quad + 2 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
             else if constexpr (kMode == kBpHalfStage)
                 pixel_pulse_half<kCheck>(quad + 2 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
@@ -654,7 +660,6 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
                 acc_r[j] = acc_i[j] = f2(0.0f, 0.0f);
             }
         }
-        if ((int)threadIdx.x < pb2) put_params(threadIdx.x, nx0, nx1, nx2, quads + 2 * pb_cap * buf2, wins + pb_cap * buf2);
         cp_async_wait_all();
         __syncthreads();
         if (pb1 > 0) transform(n1, pb1, wins + pb_cap * buf1);
