@@ -467,6 +467,7 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
     constexpr bool kSinc = kMode == kBpSinc8;
     constexpr unsigned kEb = (kMode == kBpHalfStage || kSinc) ? 8u : 16u;
     constexpr int kTapsBefore = kSinc ? 3 : 0;
+    constexpr int kPulseUnroll = kSinc ? 2 : 4;
     constexpr int kExtra = kSinc ? 7 : 1;                       // raw samples per row beyond its entries
     extern __shared__ float4 smem4[];
     constexpr int kWarps = kBpThreads / 32;
@@ -642,8 +643,9 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
             cp_async16((unsigned)__cvta_generic_to_shared(wins + pb_cap * buf2 + threadIdx.x), src + 2);
         }
         cp_async_commit();
-        // ---- pixel x pulse inner loop
-#pragma unroll 2
+        // ---- pixel x pulse inner loop (four pulses unrolled, two with sinc interpolation: measured on
+        // GB300, spotlight scene 2.861 -> 2.847 ms against two; sinc 13.19 against 13.25 ms)
+#pragma unroll(kPulseUnroll)
         for (int p = 0; p < pb; p++) {
             const int4 wv = win[p];
             const unsigned base = stage_row0 + (unsigned)(p * row_n - wv.y + kTapsBefore) * kEb;
