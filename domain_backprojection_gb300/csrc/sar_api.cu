@@ -801,17 +801,20 @@ sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double
     if (e != cudaSuccess) return cuda_status(e);
     // Pulse chunks: the copy of chunk c + 1 runs on the plan's copy stream while chunk c is range
     // compressed and backprojected (accumulating into the image) on the caller's stream.  The
-    // copy moves pulses several times faster than the kernels consume them, so the chunks grow
-    // (1/16, 3/16, 1/4 and 1/2 of the pulses): only the small first one is not overlapped.
+    // copy moves pulses about 4.5 times faster than the kernels consume them, so the chunks grow
+    // (1/16, 3/16 and 3/4 of the pulses): only the small first one is not overlapped, and each
+    // chunk's backprojection outlasts the next chunk's copy.  Every chunk adds a launch sequence
+    // and a pulse-slice tail (measured on GB300, spotlight scene: 3.52 ms with these three chunks,
+    // 3.54 ms with four (1/16, 3/16, 1/4, 1/2), 3.57 ms with five, against 3.46 ms for four chunks
+    // without their copies and 3.33 ms for one).
     cudaStream_t s = static_cast<cudaStream_t>(stream), cs = plan->copy_stream;
     const int na = r.n_pulses;
     int bounds[5] = {0, na, na, na, na};
     int chunks = 1;
     if (na >= 512) {
-        chunks = 4;
+        chunks = 3;
         bounds[1] = na / 16;
         bounds[2] = na / 4;
-        bounds[3] = na / 2;
     }
     const size_t line_bytes = (size_t)r.n_range * sizeof(float2);
     e = cudaEventRecord(plan->host_ev[0], s);                   // earlier work on the caller's stream first

@@ -128,7 +128,7 @@ sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, voi
 /* The same image formation from HOST buffers: copies raw and pos to device
  * buffers the plan owns (allocated on the first call), forms the image and
  * copies it back to image_host, then synchronises `stream`.  From 512 pulses on
- * the pulses go in 4 growing chunks: while one is range compressed and backprojected on
+ * the pulses go in 3 growing chunks: while one is range compressed and backprojected on
  * `stream` (accumulating into the image), the next is copied on a stream the
  * plan owns, so the host-to-device copy overlaps the kernels.  The image then
  * equals sar_form_image's up to the float32 summation order of the chunks.

@@ -208,13 +208,13 @@ def test_form_image_host_matches_device_path():
 
 
 def test_form_image_host_chunks_match_device_path(scenes):
-    # 1024 pulses go in 4 chunks whose copies overlap the kernels; the image equals the
+    # 1024 pulses go in 3 chunks whose copies overlap the kernels; the image equals the
     # device path's up to the float32 order of the chunk sums
     s = scenes(2)
     plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
     dev = sar.sar_form_image(plan, s["raw"], s["pos"])
     host = sar.sar_form_image_host(plan, s["raw"].cpu().pin_memory(), s["pos"].cpu().pin_memory())
-    assert sar.sar_plan_last_launches(plan) >= 4 * 4
+    assert sar.sar_plan_last_launches(plan) >= 3 * 4     # per chunk: compression, positions, prep, pixels
     sar.sar_plan_sync(plan)
     assert rel_l2(host.numpy(), dev.cpu().numpy()) <= 1e-5
 
