@@ -396,14 +396,14 @@ sar_status setup_bp(sar_plan p)
     a.nx = g.nx;
     a.ny = g.ny;
     // tile shape: the longest in azimuth (x) whose half-diagonal h stays within
-    // clamp(R_start / 100, 20 m, 32 m) and whose staged window fits the shared memory.  The range
+    // clamp(R_start / 150, 20 m, 32 m) and whose staged window fits the shared memory.  The range
     // expansion about the tile centre holds for tiles at least 100 h away (the prep kernel checks
-    // every tile and pulse), so from the start of the range window outward, and never closer than
-    // 2 km for a 20 m tile.  Shorter tiles in range stage narrower windows: 128 x 16 pixels at
+    // every tile and pulse), so down to 2/3 of the range window's start (a grid may reach nearer
+    // than the swath), and never closer than 2 km for a 20 m tile.  Shorter tiles in range stage narrower windows: 128 x 16 pixels at
     // 0.5 m stage half the samples per pulse of 64 x 32 (measured on GB300, 512 x 512 pixels, 1024
     // pulses: 0.211 against 0.238 ms).
     const double dr = kC0 / (2.0 * r.fs * r.upsample);
-    const double h_max = std::min(32.0, std::max(20.0, r.range_start / 100.0));
+    const double h_max = std::min(32.0, std::max(20.0, r.range_start / 150.0));
     // 216 KB of shared memory per SM, split between the resident CTAs: 48 pulses' parameters, the
     // rest for raw and staged rows; the kernel sizes its rows from the windows it actually stages
     const int pulses_per_batch = 48;

@@ -329,7 +329,7 @@ def test_pulse_weights():
 
 def test_tile_shape_follows_the_range_bound():
     # the plan picks the longest azimuth tile whose half-diagonal h stays within
-    # clamp(R_start / 100, 20 m, 32 m): 128 x 16 pixels at 0.5 m (h = 32 m) for the small scene's
+    # clamp(R_start / 150, 20 m, 32 m): 128 x 16 pixels at 0.5 m (h = 32 m) for the small scene's
     # 4978 m window start, 64 x 32 (h = 17.6 m) when the window starts at 1500 m
     import os
     import re
