@@ -783,7 +783,7 @@ int bp_ctas_per_sm(int smem_bytes, int mode)
 }
 
 cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s, cudaEvent_t main_begin,
-                      cudaEvent_t main_end)
+                      cudaEvent_t main_end, cudaEvent_t image_wait, cudaEvent_t image_done)
 {
     if (a.pulse_end <= a.pulse_begin) return cudaSuccess;
     const int npulse = a.pulse_end - a.pulse_begin;
@@ -795,17 +795,24 @@ cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream
     if (pe != cudaSuccess) return pe;
     const dim3 grid(a.tiles_x, a.tiles_y, slices);
     const size_t smem = bp_smem_bytes(a);
+    if (slices == 1 && image_wait && (pe = cudaStreamWaitEvent(s, image_wait, 0)) != cudaSuccess) return pe;
     if (main_begin && (pe = cudaEventRecord(main_begin, s)) != cudaSuccess) return pe;
     if (a.tile_w == 128) launch_bp_shape<128>(a, grid, smem, check_bounds, s);
     else if (a.tile_w == 64) launch_bp_shape<64>(a, grid, smem, check_bounds, s);
     else launch_bp_shape<32>(a, grid, smem, check_bounds, s);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && main_end) e = cudaEventRecord(main_end, s);
-    if (e != cudaSuccess || slices == 1) return e;
-    const int64_t npix = (int64_t)a.nx * a.ny;
-    const int blocks = (int)((npix + 255) / 256 < 4096 ? (npix + 255) / 256 : 4096);
-    bp_reduce_kernel<<<blocks, 256, 0, s>>>(a.partial, slices, npix, a.image, a.accumulate);
-    return cudaGetLastError();
+    if (e == cudaSuccess && slices > 1) {
+        const int64_t npix = (int64_t)a.nx * a.ny;
+        const int blocks = (int)((npix + 255) / 256 < 4096 ? (npix + 255) / 256 : 4096);
+        if (image_wait) e = cudaStreamWaitEvent(s, image_wait, 0);
+        if (e == cudaSuccess) {
+            bp_reduce_kernel<<<blocks, 256, 0, s>>>(a.partial, slices, npix, a.image, a.accumulate);
+            e = cudaGetLastError();
+        }
+    }
+    if (e == cudaSuccess && image_done) e = cudaEventRecord(image_done, s);
+    return e;
 }
 
 }  // namespace sar

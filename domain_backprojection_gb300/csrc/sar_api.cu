@@ -43,6 +43,9 @@ struct sar_plan_s {
     void *d_raw = nullptr, *d_pos = nullptr, *d_rc = nullptr, *d_img = nullptr;
     cudaStream_t copy_stream = nullptr;    // host path: host-to-device copies, overlapped with compute
     cudaEvent_t host_ev[5] = {};           // host path: call entry, then one per pulse chunk copied
+    cudaStream_t aux_stream = nullptr;     // host path: every other pulse chunk's kernels
+    cudaEvent_t img_ev[4] = {};            // host path: one per chunk, its last write of the image
+    float2 *d_partial2 = nullptr;          // host path: the aux stream's partial images
     int32_t last_launches = 0;
     // kernel timing (sar_plan_set_timing): event pairs around the main kernel of each call
     bool timing = false;
@@ -518,7 +521,11 @@ void free_plan(sar_plan p)
     for (cudaEvent_t e : p->ev_pool) cudaEventDestroy(e);
     for (cudaEvent_t e : p->host_ev)
         if (e) cudaEventDestroy(e);
+    for (cudaEvent_t e : p->img_ev)
+        if (e) cudaEventDestroy(e);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
+    if (p->aux_stream) cudaStreamDestroy(p->aux_stream);
+    cudaFree(p->d_partial2);
     cudaFree(p->d_tables);
     cudaFree(p->d_partial);
     cudaFree(p->d_table);
@@ -534,8 +541,13 @@ void free_plan(sar_plan p)
     delete p;
 }
 
+// With `concurrent`, the call keeps to its own pulses' rows of the parameter table, uses the
+// given partial images and orders its writes of the image after image_wait (recording
+// image_done), so that calls over disjoint pulse ranges may run on different streams at once.
 sar_status do_backproject(sar_plan plan, const void *rc, const double *pos, int32_t pulse_begin,
-                          int32_t pulse_count, void *image, int accumulate, cudaStream_t s, int layout)
+                          int32_t pulse_count, void *image, int accumulate, cudaStream_t s, int layout,
+                          bool concurrent = false, float2 *partial = nullptr, cudaEvent_t image_wait = nullptr,
+                          cudaEvent_t image_done = nullptr)
 {
     const size_t img_bytes = (size_t)plan->grid.nx * plan->grid.ny * sizeof(float2);
     if (pulse_count == 0) {
@@ -554,9 +566,13 @@ sar_status do_backproject(sar_plan plan, const void *rc, const double *pos, int3
     a.slice_len = (pulse_count + slices - 1) / slices;
     a.partial = plan->d_partial;
     a.planar = (layout == SAR_RC_POLYPHASE && plan->radar.upsample > 1) ? 1 : 0;
+    if (concurrent) {
+        a.table += (size_t)3 * a.tiles_x * a.tiles_y * pulse_begin;
+        if (partial) a.partial = partial;
+    }
     plan->last_launches += slices > 1 ? 4 : 3;
     const auto ev = timing_pair(plan, plan->ev_bp);
-    return cuda_status(sar::launch_bp(a, slices, plan->check_bounds, s, ev.first, ev.second));
+    return cuda_status(sar::launch_bp(a, slices, plan->check_bounds, s, ev.first, ev.second, image_wait, image_done));
 }
 
 }  // namespace
@@ -830,19 +846,47 @@ sar_status sar_form_image_host(sar_plan plan, const void *raw_host, const double
     if (e != cudaSuccess) return cuda_status(e);
     sar::RcArgs ra = plan->rc;
     ra.planar = 1;
+    // Chunks alternate between the caller's stream and the plan's second compute stream, so that
+    // one chunk's kernels fill the SMs the previous chunk's last wave leaves idle; only their
+    // writes of the image are ordered (chunk c's after chunk c - 1's).  Each stream has its own
+    // partial images and each chunk its own rows of the parameter table.  With kernel timing on
+    // (its events sit on one stream) the chunks run in turn on the caller's stream.
+    const bool overlap = chunks > 1 && !plan->timing && plan->bp_max_slices > 1;
+    if (overlap) {
+        if (!plan->aux_stream) e = cudaStreamCreateWithFlags(&plan->aux_stream, cudaStreamNonBlocking);
+        for (cudaEvent_t &ev : plan->img_ev)
+            if (!ev && e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (!plan->d_partial2 && e == cudaSuccess)
+            e = dev_alloc(&plan->d_partial2, (size_t)plan->bp_max_slices * img_bytes);
+        // the aux stream starts after the caller's earlier work, like the copies
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->aux_stream, plan->host_ev[0], 0);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
     int32_t launches = 0;
     for (int c = 0; c < chunks; c++) {
         const int c0 = bounds[c], cnt = bounds[c + 1] - c0;
-        e = cudaStreamWaitEvent(s, plan->host_ev[1 + c], 0);
+        const bool aux = overlap && (c & 1);
+        cudaStream_t cst = aux ? plan->aux_stream : s;
+        e = cudaStreamWaitEvent(cst, plan->host_ev[1 + c], 0);
         if (e != cudaSuccess) return cuda_status(e);
         float2 *rc = static_cast<float2 *>(plan->d_rc) + (size_t)c0 * r.n_range * r.upsample;
-        sar_status st = timed_rc(plan, ra, static_cast<const float2 *>(plan->d_raw) + (size_t)c0 * r.n_range, rc, cnt, s);
+        sar_status st = timed_rc(plan, ra, static_cast<const float2 *>(plan->d_raw) + (size_t)c0 * r.n_range, rc, cnt, cst);
         if (st != SAR_OK) return st;
         plan->last_launches = 0;
-        st = do_backproject(plan, plan->d_rc, static_cast<const double *>(plan->d_pos), c0, cnt, plan->d_img, c > 0,
-                            s, SAR_RC_POLYPHASE);
+        if (overlap)
+            st = do_backproject(plan, plan->d_rc, static_cast<const double *>(plan->d_pos), c0, cnt, plan->d_img, c > 0,
+                                cst, SAR_RC_POLYPHASE, true, aux ? plan->d_partial2 : plan->d_partial,
+                                c > 0 ? plan->img_ev[c - 1] : nullptr, plan->img_ev[c]);
+        else
+            st = do_backproject(plan, plan->d_rc, static_cast<const double *>(plan->d_pos), c0, cnt, plan->d_img, c > 0,
+                                s, SAR_RC_POLYPHASE);
         if (st != SAR_OK) return st;
         launches += 1 + plan->last_launches;
+    }
+    // the read-back follows the last chunk's image write
+    if (overlap && ((chunks - 1) & 1)) {
+        e = cudaStreamWaitEvent(s, plan->img_ev[chunks - 1], 0);
+        if (e != cudaSuccess) return cuda_status(e);
     }
     plan->last_launches = launches;
     e = cudaMemcpyAsync(image_host, plan->d_img, img_bytes, cudaMemcpyDeviceToHost, s);

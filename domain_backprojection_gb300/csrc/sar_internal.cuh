@@ -141,8 +141,13 @@ struct BpArgs {
 size_t bp_smem_bytes(const BpArgs &a);
 cudaError_t bp_configure(int smem_bytes);
 int bp_ctas_per_sm(int smem_bytes, int mode);
-// main_begin / main_end (may be null): events recorded on s right around the pixel kernel
+// main_begin / main_end (may be null): events recorded on s right around the pixel kernel.
+// image_wait (may be null): s waits for it right before the first launch that writes the image
+// (the slice sum, or the pixel kernel itself without slices); image_done (may be null) is
+// recorded on s right after that launch.  Two calls on different streams over disjoint pulses,
+// tables and partial images then overlap everywhere but in their writes of the image.
 cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream_t s,
-                      cudaEvent_t main_begin = nullptr, cudaEvent_t main_end = nullptr);
+                      cudaEvent_t main_begin = nullptr, cudaEvent_t main_end = nullptr,
+                      cudaEvent_t image_wait = nullptr, cudaEvent_t image_done = nullptr);
 
 }  // namespace sar

@@ -130,7 +130,9 @@ sar_status sar_form_image(sar_plan plan, const void *raw, const double *pos, voi
  * copies it back to image_host, then synchronises `stream`.  From 512 pulses on
  * the pulses go in 3 growing chunks: while one is range compressed and backprojected on
  * `stream` (accumulating into the image), the next is copied on a stream the
- * plan owns, so the host-to-device copy overlaps the kernels.  The image then
+ * plan owns, so the host-to-device copy overlaps the kernels; every other
+ * chunk's kernels run on a second stream the plan owns, ordered after `stream`'s
+ * earlier work, and `stream` waits for them before the read-back.  The image then
  * equals sar_form_image's up to the float32 summation order of the chunks.
  * Host buffers should be pinned for full copy bandwidth.  raw_host: [Na][Nr]
  * complex64; pos_host: [Na][3] float64; image_host: [ny][nx] complex64. */
