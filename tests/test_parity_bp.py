@@ -219,6 +219,29 @@ def test_form_image_host_chunks_match_device_path(scenes):
     assert rel_l2(host.numpy(), dev.cpu().numpy()) <= 1e-5
 
 
+
+def test_form_image_host_on_a_caller_stream(scenes):
+    # chunks alternate between the caller's stream and the plan's own: on a side stream, two calls
+    # in a row with new inputs (twice the echoes: an exactly doubled image, every step being linear
+    # and the scaling a power of two) reuse no stale chunk, and with kernel timing on (all chunks on
+    # the caller's stream, in turn) the image is bit-identical
+    s = scenes(2)
+    plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
+    raw_h = s["raw"].cpu().pin_memory()
+    raw2_h = (s["raw"] * 2).cpu().pin_memory()
+    pos_h = s["pos"].cpu().pin_memory()
+    side = torch.cuda.Stream()
+    one = sar.sar_form_image_host(plan, raw_h, pos_h, stream=side).clone()
+    two = sar.sar_form_image_host(plan, raw2_h, pos_h, stream=side).clone()
+    assert torch.equal(two, one * 2)
+    dev = sar.sar_form_image(plan, s["raw"], s["pos"])
+    assert rel_l2(one.numpy(), dev.cpu().numpy()) <= 1e-5
+    sar.sar_plan_set_timing(plan, True)
+    timed = sar.sar_form_image_host(plan, raw_h, pos_h, stream=side).clone()
+    sar.sar_plan_set_timing(plan, False)
+    assert torch.equal(timed, one)
+    sar.sar_plan_sync(plan)
+
 def test_polyphase_layout_backprojection_matches_natural():
     # the same compressed lines in either layout give the same image
     s = _small_case(70, 45, na=64)
