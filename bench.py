@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "backprojection Gpix-pulse/s + range lines/s; % FP32 and % HBM roofline"
 UNIT = "Gpix-pulse/s"
-CONFIG_ID = 3
+SCENE_ID = 3
 FLOPS_PER_PIXEL_PULSE = 30          # range 9, index 4, interpolation 6, phase 3, complex MAC 8
 PAGES_BP_GPIX_PULSE_S = 4096 * 1024 * 1024 / 0.8 / 1e9   # RTX 3080, BP only, same workload (context)
 
@@ -156,8 +156,8 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    cfg = synth.CONFIGS[CONFIG_ID]
-    scene = synth.make_scene(CONFIG_ID, device=dev)
+    cfg = synth.SCENES[SCENE_ID]
+    scene = synth.make_scene(SCENE_ID, device=dev)
     radar, grid = scene["radar"], scene["grid"]
     plan = sar.sar_plan_create(radar, grid, local_rank)
     # compressed lines in polyphase planes, as sar_form_image keeps its workspace
@@ -316,7 +316,7 @@ def profile_case(case="spotlight"):
         return
     if case == "rda":
         import dataclasses
-        scene = synth.make_scene(CONFIG_ID, device="cuda")
+        scene = synth.make_scene(SCENE_ID, device="cuda")
         cfg = scene["config"]
         plan = sar.sar_plan_create(dataclasses.replace(scene["radar"], upsample=1), None, 0)
         sar.sar_plan_set_range_doppler(plan, cfg.velocity / cfg.prf)
@@ -325,7 +325,7 @@ def profile_case(case="spotlight"):
         sar.sar_plan_sync(plan)
         print(json.dumps({"profile_case": "ok", "workload": "range-Doppler, 4096 x 4096, spotlight scene raw echoes"}))
         return
-    scene_ids = {"spotlight": CONFIG_ID, "scene1": 1, "scene2": 2, "scene4": 4}
+    scene_ids = {"spotlight": SCENE_ID, "scene1": 1, "scene2": 2, "scene4": 4}
     if case not in scene_ids:
         raise SystemExit(f"unknown profile case {case!r}")
     scene = synth.make_scene(scene_ids[case], device="cuda")
@@ -441,7 +441,7 @@ def other_scenes(dev, peaks, fp32_peak, reps=20):
     res = {}
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     for cid in (1, 2, 4):
-        cfg = synth.CONFIGS[cid]
+        cfg = synth.SCENES[cid]
         scene = synth.make_scene(cid, device=dev)
         radar, grid = scene["radar"], scene["grid"]
         plan = sar.sar_plan_create(radar, grid, dev.index)
@@ -562,7 +562,7 @@ def run_reference(args, rank, world, local_rank):
 
     if rank != 0:
         return None
-    scene = synth.make_scene(CONFIG_ID, device="cuda" if torch.cuda.is_available() else "cpu")
+    scene = synth.make_scene(SCENE_ID, device="cuda" if torch.cuda.is_available() else "cpu")
     per_step = max(1.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         cpu_baseline(scene, budget_s=per_step)
@@ -570,7 +570,7 @@ def run_reference(args, rank, world, local_rank):
     vals = [r["value"] for r in runs]
     cb = dict(runs[-1])
     v = statistics.median(vals)
-    cfg = synth.CONFIGS[CONFIG_ID]
+    cfg = synth.SCENES[SCENE_ID]
     ms = cfg.pixel_pulses / (v * 1e9) * 1e3
     cb["value"] = round(v, 5)
     return {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": UNIT, "n_gpus": world,

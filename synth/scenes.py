@@ -122,7 +122,7 @@ def _spotlight_prf(na, v, rc, aperture_deg):
     return na * v / length
 
 
-CONFIGS = {
+SCENES = {
     1: SceneConfig("tiny-stripmap", 256, 1024, 8, 300.0, 128, 128, 0.5, 3, False, True, 20.0,
                    seed=1001, fixed_target_offsets=((0, 0), (-20, 16), (24, -28))),
     2: SceneConfig("small-stripmap", 1024, 2048, 8, 1200.0, 512, 512, 0.5, 16, True, False, 10.0,
@@ -289,7 +289,7 @@ def make_scene(cfg_id, device="cpu", with_clutter: bool = True, with_noise: bool
     """Build one of the benchmark scenes.  Returns a dict with
     raw [Na][Nr] complex64, pos [Na][3] float64, radar, grid, config, and the
     point targets (xyz, amplitude, pixel index or None)."""
-    cfg = CONFIGS[cfg_id] if isinstance(cfg_id, int) else cfg_id
+    cfg = SCENES[cfg_id] if isinstance(cfg_id, int) else cfg_id
     radar = cfg.radar()
     grid = cfg.grid()
     pos = track(cfg, device)

@@ -22,7 +22,7 @@ from synth.scenes import add_echoes  # noqa: E402
 
 
 def compute():
-    cfg = dataclasses.replace(synth.CONFIGS[1], n_pulses=32, prf=300.0 / 8)
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=32, prf=300.0 / 8)
     radar, grid = cfg.radar(), cfg.grid()
     pos = synth.track(cfg)
     xyz = torch.tensor([[grid.x0 + 64 * grid.dx, grid.y0 + 64 * grid.dy, 0.0]], dtype=torch.float64)

@@ -13,8 +13,8 @@ import domain_backprojection_gb300 as sar
 import synth
 from domain_backprojection_gb300 import _binding as B
 
-RADAR = synth.CONFIGS[1].radar()
-GRID = synth.CONFIGS[1].grid()
+RADAR = synth.SCENES[1].radar()
+GRID = synth.SCENES[1].grid()
 
 
 def _create(radar=RADAR, grid=GRID, device=0, out=True):

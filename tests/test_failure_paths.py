@@ -47,7 +47,7 @@ def test_wait_that_runs_out_reports_timeout_and_context_survives(monkeypatch):
 
 
 def test_injected_allocation_failures(monkeypatch):
-    cfg = dataclasses.replace(synth.CONFIGS[1], n_pulses=32, nx=16, ny=16)
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=32, nx=16, ny=16)
     radar, grid = cfg.radar(), cfg.grid()
     monkeypatch.setenv("SAR_INJECT_ALLOC_FAILURE", "1")
     with pytest.raises(sar.SarError) as e:                     # the plan's first allocation
@@ -62,7 +62,7 @@ def test_injected_allocation_failures(monkeypatch):
         sar.sar_form_image_host(plan, s["raw"].cpu().pin_memory(), s["pos"].cpu().pin_memory(), img)
     assert e.value.status == SAR_ERR_NO_MEMORY
     monkeypatch.delenv("SAR_INJECT_ALLOC_FAILURE")
-    rd_plan = sar.sar_plan_create(dataclasses.replace(synth.CONFIGS[2].radar(), upsample=1, n_pulses=512), None, 0)
+    rd_plan = sar.sar_plan_create(dataclasses.replace(synth.SCENES[2].radar(), upsample=1, n_pulses=512), None, 0)
     monkeypatch.setenv("SAR_INJECT_ALLOC_FAILURE", "1")
     with pytest.raises(sar.SarError) as e:                     # the range-Doppler tables
         sar.sar_plan_set_range_doppler(rd_plan, 0.1)
@@ -82,7 +82,7 @@ def test_log_trace_on_request():
     import os
     import subprocess
     import sys
-    code = ("import synth, domain_backprojection_gb300 as sar; c = synth.CONFIGS[1]; "
+    code = ("import synth, domain_backprojection_gb300 as sar; c = synth.SCENES[1]; "
             "p = sar.sar_plan_create(c.radar(), c.grid(), 0)")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     env = dict(os.environ, SAR_LOG="1")

@@ -20,8 +20,8 @@ def test_pixel_pulse_counts_match_printed_examples():
     for ex in _facts()["pixel_pulse_examples"]:
         assert abs(ex["n_pulses"] * ex["nx"] * ex["ny"] / ex["printed"] - 1) < 0.02
     # the benchmark scenes sized like the pages' examples
-    assert synth.CONFIGS[3].pixel_pulses == 4096 * 1024 * 1024
-    assert synth.CONFIGS[4].pixel_pulses == 16384 * 2048 * 2048
+    assert synth.SCENES[3].pixel_pulses == 4096 * 1024 * 1024
+    assert synth.SCENES[4].pixel_pulses == 16384 * 2048 * 2048
 
 
 def test_sinc_first_sidelobe_is_near_printed_value():

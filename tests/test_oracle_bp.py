@@ -15,7 +15,7 @@ import oracle
 import synth
 from synth.scenes import add_echoes, chirp_count
 
-CFG1 = synth.CONFIGS[1]
+CFG1 = synth.SCENES[1]
 
 
 def single_target_scene(cfg, pix, amp=1.0 + 0j, noise=False):

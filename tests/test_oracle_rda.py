@@ -20,7 +20,7 @@ from synth.scenes import add_echoes, chirp_count
 
 def _target(na, prf, n_t, di, amp=0.8 * np.exp(1j * 0.4)):
     """One scatterer on range bin n_range/2 + di at the along-track position of pulse n_t."""
-    cfg = dataclasses.replace(synth.CONFIGS[2], n_pulses=na, prf=prf, upsample=1)
+    cfg = dataclasses.replace(synth.SCENES[2], n_pulses=na, prf=prf, upsample=1)
     radar, pos = cfg.radar(), synth.track(cfg)
     dr = synth.C0 / (2 * radar.fs)
     i_t = cfg.n_range // 2 + di

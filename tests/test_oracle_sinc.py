@@ -71,7 +71,7 @@ def _scene(cfg, pix, amp):
 
 
 def test_point_target_gain_with_sinc():
-    cfg = dataclasses.replace(synth.CONFIGS[1], nx=32, ny=32)
+    cfg = dataclasses.replace(synth.SCENES[1], nx=32, ny=32)
     radar, grid, pos, raw = _scene(cfg, (16, 12), 0.8 * np.exp(1j * 0.4))
     rc = oracle.range_compress(radar, raw)
     img = oracle.backproject(radar, grid, rc, pos, interp=SINC)
@@ -87,7 +87,7 @@ def test_brute_force_correlation_closer_than_linear(upsample):
     # the exact-delay time-domain correlation (no FFT, no interpolation) as in the linear pin; sinc
     # interpolation of the same compressed lines must land closer to it than linear interpolation,
     # and at x2 upsampling far closer
-    cfg = dataclasses.replace(synth.CONFIGS[1], n_pulses=16, prf=300.0 / 16 * 2, n_range=1024, nx=16, ny=16,
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=16, prf=300.0 / 16 * 2, n_range=1024, nx=16, ny=16,
                               upsample=upsample)
     radar, grid = cfg.radar(), cfg.grid()
     pos = synth.track(cfg)

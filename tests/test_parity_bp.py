@@ -71,7 +71,7 @@ def test_form_image_full_size_sampled(scenes, cfg, n_random):
 
 
 def _small_case(nx=45, ny=70, na=96):
-    cfg = dataclasses.replace(synth.CONFIGS[1], n_pulses=na, prf=300.0 * na / 256, nx=nx, ny=ny,
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=na, prf=300.0 * na / 256, nx=nx, ny=ny,
                               fixed_target_offsets=((0, 0), (-9, 11), (13, -20)))
     return synth.make_scene(cfg, device="cuda")
 
@@ -297,7 +297,7 @@ def test_form_image_captures_into_a_cuda_graph():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         sar.sar_form_image(plan, raw, pos, image=img, workspace=ws)
-    other = synth.make_scene(dataclasses.replace(synth.CONFIGS[1], seed=91), device="cuda")
+    other = synth.make_scene(dataclasses.replace(synth.SCENES[1], seed=91), device="cuda")
     for scene in (s, other):
         raw.copy_(scene["raw"])
         pos.copy_(scene["pos"])
@@ -358,7 +358,7 @@ def test_tile_shape_follows_the_range_bound():
     import re
     import subprocess
     import sys
-    code = ("import dataclasses, synth, domain_backprojection_gb300 as sar; c = synth.CONFIGS[2]; "
+    code = ("import dataclasses, synth, domain_backprojection_gb300 as sar; c = synth.SCENES[2]; "
             "sar.sar_plan_create(c.radar(), c.grid(), 0); "
             "sar.sar_plan_create(dataclasses.replace(c.radar(), range_start=1500.0), c.grid(), 0)")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))

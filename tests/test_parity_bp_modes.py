@@ -86,7 +86,7 @@ def test_compensated_sums_no_worse_on_the_long_aperture(scene_cache):
 def test_mode_pulse_weights_blocks_and_bounds(mode, monkeypatch):
     # pulse weights, two pulse blocks accumulated, and the bounds-checked build (no flag raised)
     monkeypatch.setenv("SAR_CHECK_BOUNDS", "1")
-    cfg = dataclasses.replace(synth.CONFIGS[1], n_pulses=96, prf=300.0 * 96 / 256, nx=45, ny=70,
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=96, prf=300.0 * 96 / 256, nx=45, ny=70,
                               fixed_target_offsets=((0, 0), (-9, 11), (13, -20)))
     s = synth.make_scene(cfg, device="cuda")
     plan = _plan(s, mode)
@@ -103,7 +103,7 @@ def test_mode_pulse_weights_blocks_and_bounds(mode, monkeypatch):
 
 def test_sinc_at_low_upsampling(scene_cache):
     # sinc interpolation of x2 lines: compared with the oracle's sinc image of the same lines
-    cfg = dataclasses.replace(synth.CONFIGS[2], upsample=2)
+    cfg = dataclasses.replace(synth.SCENES[2], upsample=2)
     s = synth.make_scene(cfg, device="cuda")
     plan = _plan(s, "sinc8")
     img = sar.sar_form_image(plan, s["raw"], s["pos"])
@@ -115,7 +115,7 @@ def test_sinc_at_low_upsampling(scene_cache):
 
 
 def test_option_setters():
-    s = synth.make_scene(dataclasses.replace(synth.CONFIGS[1], n_pulses=16, nx=8, ny=8), device="cuda")
+    s = synth.make_scene(dataclasses.replace(synth.SCENES[1], n_pulses=16, nx=8, ny=8), device="cuda")
     plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
     sar.sar_plan_set_interpolation(plan, sar.SAR_INTERP_SINC8)
     with pytest.raises(sar.SarError) as e:                       # a second non-default option

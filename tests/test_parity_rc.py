@@ -73,7 +73,7 @@ def test_rc_sweep_full_size(nr):
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_rc_scene_configs_sampled(scene_cache, cfg):
-    c = synth.CONFIGS[cfg]
+    c = synth.SCENES[cfg]
     scene = scene_cache(cfg)
     plan = sar.sar_plan_create(scene["radar"], None, 0)
     rc = sar.sar_range_compress(plan, scene["raw"])
@@ -168,7 +168,7 @@ def test_image_from_bluestein_length_lines():
     # (U = 8, natural and polyphase layouts) and backprojection against the oracle
     import dataclasses
     from helpers import IMG_TOL
-    cfg = dataclasses.replace(synth.CONFIGS[1], n_pulses=96, prf=300.0 * 96 / 256, n_range=1026, nx=45, ny=70,
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=96, prf=300.0 * 96 / 256, n_range=1026, nx=45, ny=70,
                               fixed_target_offsets=((0, 0), (-9, 11), (13, -20)))
     s = synth.make_scene(cfg, device="cuda")
     plan = sar.sar_plan_create(s["radar"], s["grid"], 0)

@@ -62,7 +62,7 @@ def test_range_doppler_matches_oracle(scene_cache, cfg):
 
 
 def test_point_target_phase_and_position():
-    cfg = dataclasses.replace(synth.CONFIGS[2], n_pulses=1024, prf=100.0 / 0.28, upsample=1)
+    cfg = dataclasses.replace(synth.SCENES[2], n_pulses=1024, prf=100.0 / 0.28, upsample=1)
     radar, pos = cfg.radar(), synth.track(cfg)
     du, dr = cfg.velocity / cfg.prf, synth.C0 / (2 * radar.fs)
     i_t, n_t = cfg.n_range // 2 - 7, 500
@@ -80,7 +80,7 @@ def test_point_target_phase_and_position():
 
 
 def test_non_power_of_two_range_and_smallest_aperture():
-    cfg = dataclasses.replace(synth.CONFIGS[2], n_pulses=512, prf=600.0, n_range=1000, upsample=1)
+    cfg = dataclasses.replace(synth.SCENES[2], n_pulses=512, prf=600.0, n_range=1000, upsample=1)
     radar, pos = cfg.radar(), synth.track(cfg)
     g = torch.Generator().manual_seed(9)
     raw = torch.complex(torch.randn(512, 1000, generator=g), torch.randn(512, 1000, generator=g)) * 0.1
@@ -99,7 +99,7 @@ def test_non_power_of_two_range_and_smallest_aperture():
 @pytest.mark.parametrize("na,nr", [(2048, 512), (8192, 768)])
 def test_other_aperture_lengths(na, nr):
     # the 2048- and 8192-point azimuth transforms (one CTA per range bin of N/16 threads)
-    cfg = dataclasses.replace(synth.CONFIGS[2], n_pulses=na, prf=1200.0 * na / 1024, n_range=nr, upsample=1)
+    cfg = dataclasses.replace(synth.SCENES[2], n_pulses=na, prf=1200.0 * na / 1024, n_range=nr, upsample=1)
     radar, pos = cfg.radar(), synth.track(cfg)
     g = torch.Generator().manual_seed(na)
     raw = torch.complex(torch.randn(na, nr, generator=g), torch.randn(na, nr, generator=g)) * 0.05
@@ -118,7 +118,7 @@ def test_other_aperture_lengths(na, nr):
 def test_range_doppler_captures_into_a_cuda_graph():
     # sar_range_doppler enqueues its launches with no allocation or synchronisation once the plan's
     # tables exist: capture it once, replay it on new echoes copied into the captured buffer
-    cfg = dataclasses.replace(synth.CONFIGS[2], n_pulses=512, prf=600.0, n_range=1024, upsample=1)
+    cfg = dataclasses.replace(synth.SCENES[2], n_pulses=512, prf=600.0, n_range=1024, upsample=1)
     radar = cfg.radar()
     plan = sar.sar_plan_create(radar, None, 0)
     sar.sar_plan_set_range_doppler(plan, cfg.velocity / cfg.prf)
@@ -145,7 +145,7 @@ def test_range_doppler_captures_into_a_cuda_graph():
 
 
 def test_range_doppler_arguments():
-    radar = dataclasses.replace(synth.CONFIGS[2].radar(), upsample=1)
+    radar = dataclasses.replace(synth.SCENES[2].radar(), upsample=1)
     plan = sar.sar_plan_create(radar, None, 0)
     L = sar.lib()
     n = ctypes.c_size_t()

@@ -33,7 +33,7 @@ def _entry():
 def test_noalloc_matches_form_image_on_two_calls_in_a_row():
     noalloc = _entry()
     base = synth.make_scene(1, device="cuda")            # 256 x 8192 compressed samples = 16 MiB of scratch
-    other = synth.make_scene(dataclasses.replace(synth.CONFIGS[1], seed=77,
+    other = synth.make_scene(dataclasses.replace(synth.SCENES[1], seed=77,
                                                  fixed_target_offsets=((5, -7), (30, 12))), device="cuda")
     plan = sar.sar_plan_create(base["radar"], base["grid"], 0)
     stream = torch.cuda.current_stream()
