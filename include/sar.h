@@ -116,8 +116,8 @@ sar_status sar_range_compress(sar_plan plan, const void *raw, void *rc, int64_t 
  * SAR_ERR_UNSUPPORTED if a tile came closer to the antenna than the
  * expansion allows (range below 100 tile half-diagonals).  Tiles hold 2048
  * pixels (128 x 16, 64 x 32 or 32 x 64, the longest in x whose half-diagonal
- * stays within clamp(range_start / 150, 20 m, 32 m)), so any grid from 2/3 of
- * range_start outward, and from 2 km outward in every case, is in range. */
+ * stays within clamp(range_start / 150, 20 m, 32 m)), so every tile centre at
+ * max(2 km, 2/3 range_start) or beyond is in range. */
 sar_status sar_backproject(sar_plan plan, const void *rc, const double *pos, int32_t pulse_begin,
                            int32_t pulse_count, void *image, int accumulate, void *stream);
 
