@@ -358,21 +358,30 @@ sar_status setup_rc(sar_plan p)
 }
 
 // Pulse slices for a backprojection of `pulses` pulses: the tiles x slices work units should fill
-// the resident CTA slots in whole waves.  A larger count is taken only when it cuts the estimated
-// time (waves per unit of work) by at least 3%; each slice keeps at least 16 pulses.
+// the resident CTA slots in whole waves without making the slices so short that the CTAs' fixed
+// cost dominates; each slice keeps at least 16 pulses.
 int bp_pick_slices(sar_plan p, int pulses)
 {
+    // Time of a call with S slices ~ waves(S) * (pulses / S + P0): the CTAs of tiles * S units run
+    // in waves of `slots`, each CTA walks pulses / S pulses, and P0 ~ 8 pulses' worth of time is
+    // a CTA's fixed cost (its first batches' parameters, gather and barriers).  Fewer slices win
+    // ties within 0.5% (less partial-image traffic).  For 512 tiles on 456 slots and 4096 pulses
+    // that is 8 slices (9 waves of 512-pulse CTAs) rather than 7 (8 waves of 585).
+    constexpr double kCtaFixedPulses = 8.0;
     const long long tiles = (long long)p->bp.tiles_x * p->bp.tiles_y;
     const long long slots = p->bp_slots > 0 ? p->bp_slots : 1;
     int cap = pulses / 16;
     if (cap > sar::kBpMaxSlices) cap = sar::kBpMaxSlices;
+    auto cost = [&](int sl) {
+        return (double)((tiles * sl + slots - 1) / slots) * ((double)pulses / sl + kCtaFixedPulses);
+    };
     int best = 1;
-    double best_cost = (double)((tiles + slots - 1) / slots);
+    double best_cost = cost(1);
     for (int sl = 2; sl <= cap; sl++) {
-        const double cost = (double)((tiles * sl + slots - 1) / slots) / sl;
-        if (cost < 0.97 * best_cost) {
+        const double c = cost(sl);
+        if (c < 0.995 * best_cost) {
             best = sl;
-            best_cost = cost;
+            best_cost = c;
         }
     }
     return best;
