@@ -19,6 +19,7 @@ problems, weak scaling, no collective on the data path).
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -256,7 +257,8 @@ def run_ours(args, rank, world, local_rank):
                         "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
                         "frac": round(rc_gbs / float(peaks.get("hbm_gbs", 6800.0)), 4),
                         "traffic": kernel_traffic(rc_name.split("<")[0]),
-                        "peak_source": peak_src, "algorithmic_bytes_per_line": 8 * n_range * (1 + U)},
+                        "peak_source": peak_src, "algorithmic_bytes_per_line": 8 * n_range * (1 + U),
+                        "context_tflops": round(rc_flops_per_line(n_range, U) * cfg.n_pulses / (rc_ms * 1e-3) / 1e12, 3)},
         "clocks": clk,
         "e2e": {"value": round(whole_job_rate(pp, world, e2e_s) / 1e9, 3), "unit": UNIT,
                 "h2d_bytes_per_step": raw_h.numel() * 8 + pos_h.numel() * 8,
@@ -276,6 +278,13 @@ def run_ours(args, rank, world, local_rank):
         # the same oracle on one core, for comparison with single-thread figures
         out["cpu_baseline_1thread"] = cpu_baseline(scene, budget_s=max(2.0, args.cpu_seconds / 3), threads=1)
     return out
+
+
+def rc_flops_per_line(nr, upsample=1):
+    """Conventional flop count of one compressed line, reported as context beside the HBM roofline:
+    5 N log2 N per N-point transform for the forward transform and the U inverse ones, plus 6 N for
+    the matched-filter product."""
+    return 5.0 * nr * math.log2(nr) * (1 + upsample) + 6.0 * nr
 
 
 def rc_kernel_name(nr, upsample=1):

@@ -69,3 +69,9 @@ def test_clock_summary_reads_reasons():
     out = s.summary()
     assert out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0 and out["samples"] == 3
     assert out["reasons"] == ["sw_power_cap"]
+
+
+def test_rc_context_flops():
+    # 5 N log2 N per transform, (1 + U) transforms, plus the 6 N flops of the filter product
+    assert bench.rc_flops_per_line(4096, 8) == 5 * 4096 * 12 * 9 + 6 * 4096
+    assert bench.rc_flops_per_line(1024, 1) == 5 * 1024 * 10 * 2 + 6 * 1024
