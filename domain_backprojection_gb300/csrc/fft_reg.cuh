@@ -196,6 +196,43 @@ template <bool kInv> struct Dft<16, kInv> {
     }
 };
 
+// 32 = 2 x 16: DFT16 of the even and of the odd samples, the odd ones turned by exp(-2 pi i k / 32),
+// then sums and differences (forward only; the 8192-point line kernel inverts by the conjugate
+// identity).
+template <> struct Dft<32, false> {
+    static __device__ __forceinline__ void run(float2 *a)
+    {
+        // cos and sin of 2 pi k / 32, k = 0 .. 8
+        constexpr float c[9] = {1.0f, 0.98078528040323044913f, 0.92387953251128675613f, 0.83146961230254523708f,
+                                0.70710678118654752440f, 0.55557023301960222474f, 0.38268343236508977173f,
+                                0.19509032201612826785f, 0.0f};
+        float2 e[16], o[16];
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+            e[k] = a[2 * k];
+            o[k] = a[2 * k + 1];
+        }
+        Dft<16>::run(e);
+        Dft<16>::run(o);
+        // o_k *= exp(-2 pi i k / 32) = cos - i sin, with both taken from the first quarter wave
+#pragma unroll
+        for (int k = 1; k < 16; k++) {
+            if (k == 8) {
+                o[k] = mul_minus_i(o[k]);
+            } else {
+                const float cs = k < 8 ? c[k] : -c[16 - k];   // cos(2 pi k / 32)
+                const float sn = k < 8 ? c[8 - k] : c[k - 8]; // sin(2 pi k / 32)
+                o[k] = cmul(o[k], make_float2(cs, -sn));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+            a[k] = cadd(e[k], o[k]);
+            a[k + 16] = csub(e[k], o[k]);
+        }
+    }
+};
+
 // ---------------------------------------------------------------------------
 // Register-resident transforms for power-of-two lines, Nr = 512 ... 8192.
 // Each of the Nr/16 threads holds 16 elements, element t + T p in slot p

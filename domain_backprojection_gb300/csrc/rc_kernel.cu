@@ -16,8 +16,10 @@
 // per-u phase ramp (a polyphase split of the output index).
 //
 // Kernels by line length Nr (launch_rc picks one):
-//   - rc_reg_kernel<N, U>1>: powers of two 512 .. 8192, register-resident radix-16
-//     transforms (fft_reg.cuh); 8192-point lines staged by bulk copy;
+//   - rc_reg_kernel<N, U>1>: powers of two 512 .. 8192 (8192 only with upsampling),
+//     register-resident radix-16 transforms (fft_reg.cuh); 8192-point lines staged by
+//     bulk copy;
+//   - rc_reg32_kernel: Nr = 8192 without upsampling, 32 elements per thread;
 //   - rc_mixed6000_kernel<U>1>: Nr = 6000, register-resident radix 10/10/10/6;
 //   - rc_fused_kernel: other even 2^a 3^b 5^c lengths, mixed-radix Stockham passes
 //     (16, 8, 5, 4, 3, 2) between two shared-memory buffers, the spectrum in a third;
@@ -362,14 +364,23 @@ __global__ void __launch_bounds__(N / 16, (rc_reg_min_ctas<N, kMulti>()))
 }
 
 // ---------------------------------------------------------------------------
-// Register-resident transform for Nr = 6000 = 2^4 3 5^3 (the non-power-of-two
-// line of the range-only sweep): 200 threads of 30 elements, element t + T p in
-// slot p (T = 200), and four Stockham passes of radix 10, 10, 10 and 6, each
-// thread running 30 / R butterflies per pass.  As in the power-of-two kernel,
-// the first pass reads registers, the last leaves its output in registers in
-// the t + T p layout, and the passes in between exchange through shared memory.
+// Register-resident transforms with E elements per thread, element t + T p in
+// slot p (T = N / E), each thread running E / R butterflies per pass:
+//   - Nr = 6000 = 2^4 3 5^3 (the non-power-of-two line of the range-only sweep):
+//     200 threads of 30 elements, four passes of radix 10, 10, 10 and 6;
+//   - Nr = 8192 without upsampling: 256 threads of 32 elements, three passes of
+//     radix 16, 16 and 32 (two exchanges, against three for 16 elements per
+//     thread).
+// As in the 16-element kernel, the first pass reads registers, the last leaves
+// its output in registers in the t + T p layout, and the passes in between
+// exchange through shared memory.  kPad32 adds one entry of padding per 32 to
+// the exchange indices, which keeps the radix-32 pass's stride-32 reads free of
+// bank conflicts.
 // ---------------------------------------------------------------------------
-template <int N, int E, int R, int L, bool kFirst, bool kLast, bool kOneBuf>
+template <bool kPad32>
+__device__ __forceinline__ int xpad(int i) { return kPad32 ? i + (i >> 5) : i; }
+
+template <int N, int E, int R, int L, bool kFirst, bool kLast, bool kOneBuf, bool kPad32 = false>
 __device__ __forceinline__ void mixed_pass(float2 (&x)[E], const float2 *src, float2 *dst, const float2 *__restrict__ tw)
 {
     constexpr int T = N / E, SP = N / (L * R), NB = E / R;
@@ -390,7 +401,7 @@ __device__ __forceinline__ void mixed_pass(float2 (&x)[E], const float2 *src, fl
             const int b = t + T * i;
             const int jp = b % SP, kp = b / SP;
 #pragma unroll
-            for (int p = 0; p < R; p++) x[i * R + p] = src[kp * SP * R + jp + SP * p];
+            for (int p = 0; p < R; p++) x[i * R + p] = src[xpad<kPad32>(kp * SP * R + jp + SP * p)];
         }
         if (kOneBuf && !kLast) __syncthreads();
     }
@@ -407,7 +418,7 @@ __device__ __forceinline__ void mixed_pass(float2 (&x)[E], const float2 *src, fl
         Dft<R>::run(x + i * R);
         if (!kLast) {
 #pragma unroll
-            for (int q = 0; q < R; q++) dst[(kp + L * q) * SP + jp] = x[i * R + q];
+            for (int q = 0; q < R; q++) dst[xpad<kPad32>((kp + L * q) * SP + jp)] = x[i * R + q];
         }
     }
     if (!kLast) __syncthreads();
@@ -553,6 +564,54 @@ __global__ void __launch_bounds__(200, kMulti ? kRcMixedCtas : 2) rc_mixed6000_k
     }
 }
 
+// 8192-point lines without upsampling: 256 threads of 32 elements (one CTA per line, 2 per SM at
+// 128 registers), passes of radix 16, 16 and 32 with two exchanges through one padded buffer, the
+// inverse transform by the conjugate identity (one copy of the transform code in a two-trip loop).
+// Measured on GB300, 4096 lines: 0.167 ms against 0.191 ms for 512 threads of 16 elements (three
+// exchanges, one 16-warp CTA per SM with bulk-copy staging).  Each CTA asks L2 for the line of the
+// CTA that will take its place (args.prefetch_ahead lines on, the kernel's resident CTAs): the
+// load of a new line then finds its data in L2 (0.174 -> 0.167 ms).
+constexpr int kRc8192Threads = 256, kRc8192Elems = 32;
+
+__host__ __device__ constexpr size_t rc8192_smem() { return (size_t)(8192 + 8192 / 32) * sizeof(float2); }
+
+__global__ void __launch_bounds__(kRc8192Threads, 2)
+    rc_reg32_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc, int64_t n_lines, RcArgs args)
+{
+    constexpr int N = 8192, E = kRc8192Elems, T = kRc8192Threads;
+    extern __shared__ float4 smem4[];
+    float2 *buf = reinterpret_cast<float2 *>(smem4);
+    const int t = threadIdx.x;
+    for (int64_t line = blockIdx.x; line < n_lines; line += gridDim.x) {
+        const int64_t ahead = line + args.prefetch_ahead;
+        if (ahead < n_lines) {
+            // two 128-byte lines per thread cover the 64 KB raw line
+            const float2 *q = raw + ahead * N + 16 * t;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(q + 16 * T));
+        }
+        float2 x[E];
+        const float2 *src = raw + line * N;
+#pragma unroll
+        for (int p = 0; p < E; p++) x[p] = ld_raw(src + t + T * p);
+#pragma unroll 1
+        for (int trip = 0; trip < 2; trip++) {
+            mixed_pass<N, E, 16, 1, true, false, true, true>(x, nullptr, buf, args.tw);
+            mixed_pass<N, E, 16, 16, false, false, true, true>(x, buf, buf, args.tw);
+            mixed_pass<N, E, 32, 256, false, true, true, true>(x, buf, nullptr, args.tw);
+            __syncthreads();                                    // the buffer is free for the next transform
+            if (trip == 0) {
+                // filter (with the IDFT's 1 / Nr) and conjugate
+#pragma unroll
+                for (int p = 0; p < E; p++) x[p] = cconj(cmul(x[p], __ldg(args.h + t + T * p)));
+            }
+        }
+        float2 *out = rc + line * N;
+#pragma unroll
+        for (int p = 0; p < E; p++) out[t + T * p] = cconj(x[p]);
+    }
+}
+
 // Bluestein lines without upsampling, register-resident: the four M-point transforms of a line
 // (M = 512 .. 8192) are reg_dft passes over the thread's 16 elements t + T p (T = M / 16), the
 // line's samples in the first N positions.
@@ -671,8 +730,9 @@ cudaError_t rc_configure(int)
     if (e == cudaSuccess) e = set_reg_smem<2048, true>();
     if (e == cudaSuccess) e = set_reg_smem<4096, false>();
     if (e == cudaSuccess) e = set_reg_smem<4096, true>();
-    if (e == cudaSuccess) e = set_reg_smem<8192, false>();
     if (e == cudaSuccess) e = set_reg_smem<8192, true>();
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_reg32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rc8192_smem());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(rc_mixed6000_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)rc_mixed_smem(false));
@@ -680,6 +740,12 @@ cudaError_t rc_configure(int)
         e = cudaFuncSetAttribute(rc_mixed6000_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)rc_mixed_smem(true));
     return e;
+}
+
+int rc_prefetch_ahead(int n, int u, int dev)
+{
+    if (n == 8192 && u == 1) return resident(rc_reg32_kernel, kRc8192Threads, rc8192_smem(), dev);
+    return 0;
 }
 
 bool rc_has_reg_path(int n) { return n == 512 || n == 1024 || n == 2048 || n == 4096 || n == 8192; }
@@ -692,7 +758,7 @@ int rc_resident_ctas(int n, int u, int dev)
     case 1024: return multi ? reg_resident<1024, true>(dev) : reg_resident<1024, false>(dev);
     case 2048: return multi ? reg_resident<2048, true>(dev) : reg_resident<2048, false>(dev);
     case 4096: return multi ? reg_resident<4096, true>(dev) : reg_resident<4096, false>(dev);
-    case 8192: return multi ? reg_resident<8192, true>(dev) : reg_resident<8192, false>(dev);
+    case 8192: return multi ? reg_resident<8192, true>(dev) : 1 << 20;    // U = 1: one CTA per line
     case 6000:
         if (!rc_mixed_staged(multi)) return 1 << 20;
         return multi ? resident(rc_mixed6000_kernel<true>, 200, rc_mixed_smem(true), dev)
@@ -705,7 +771,7 @@ template <int N>
 static void launch_reg(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, unsigned grid, cudaStream_t s)
 {
     if (a.u > 1) rc_reg_kernel<N, true><<<grid, N / 16, rc_reg_smem<N, true>(), s>>>(raw, rc, n_lines, a);
-    else rc_reg_kernel<N, false><<<grid, N / 16, rc_reg_smem<N, false>(), s>>>(raw, rc, n_lines, a);
+    else if constexpr (N != 8192) rc_reg_kernel<N, false><<<grid, N / 16, rc_reg_smem<N, false>(), s>>>(raw, rc, n_lines, a);
 }
 
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s)
@@ -719,7 +785,10 @@ cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_
     case 1024: launch_reg<1024>(a, raw, rc, n_lines, grid, s); break;
     case 2048: launch_reg<2048>(a, raw, rc, n_lines, grid, s); break;
     case 4096: launch_reg<4096>(a, raw, rc, n_lines, grid, s); break;
-    case 8192: launch_reg<8192>(a, raw, rc, n_lines, grid, s); break;
+    case 8192:
+        if (a.u == 1) rc_reg32_kernel<<<grid, kRc8192Threads, rc8192_smem(), s>>>(raw, rc, n_lines, a);
+        else launch_reg<8192>(a, raw, rc, n_lines, grid, s);
+        break;
     case 6000:
         if (a.u == 1) rc_mixed6000_kernel<false><<<grid, 200, rc_mixed_smem(false), s>>>(raw, rc, n_lines, a);
         else rc_mixed6000_kernel<true><<<grid, 200, rc_mixed_smem(true), s>>>(raw, rc, n_lines, a);

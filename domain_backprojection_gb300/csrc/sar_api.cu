@@ -354,6 +354,7 @@ sar_status setup_rc(sar_plan p)
     e = sar::rc_configure(n);
     if (e != cudaSuccess) return cuda_status(e);
     a.max_ctas = sar::rc_resident_ctas(n, U, p->device);
+    a.prefetch_ahead = sar::rc_prefetch_ahead(n, U, p->device);
     return a.max_ctas > 0 ? SAR_OK : SAR_ERR_CUDA;
 }
 
@@ -1094,7 +1095,7 @@ extern "C" sar_status sar_form_image_noalloc(sar_plan plan, const void *raw, con
     plan->last_launches = 1;
     sar::RcArgs ra = plan->rc;
     ra.planar = 1;
-    st = cuda_status(sar::launch_rc(ra, static_cast<const float2 *>(raw), scratch, plan->radar.n_pulses, s));
+    st = timed_rc(plan, ra, static_cast<const float2 *>(raw), scratch, plan->radar.n_pulses, s);
     if (st != SAR_OK) return st;
     return do_backproject(plan, scratch, pos, 0, plan->radar.n_pulses, image, 0, s, SAR_RC_POLYPHASE);
 }

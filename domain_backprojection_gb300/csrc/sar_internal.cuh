@@ -48,6 +48,7 @@ struct RcArgs {
     unsigned long long wait_limit_ns;   // bound of the staged kernels' waits (kWaitLimitNs unless the
                                         // SAR_WAIT_LIMIT_NS knob sets another; 0 = test once)
     int max_ctas;            // CTAs of the line kernel resident on the whole device (its grid cap)
+    int prefetch_ahead;      // lines ahead whose raw samples a line kernel asks L2 for (0: none)
     int *err;                // device error word
 };
 
@@ -58,6 +59,9 @@ size_t rc_bluestein_smem(int n, int u, int m);
 cudaError_t rc_configure(int n);
 // CTAs of the line kernel for (n, u) that fit on device `dev` at once (0 on error).
 int rc_resident_ctas(int n, int u, int dev);
+// Lines ahead of its own whose raw samples a one-CTA-per-line kernel prefetches into L2 (the CTAs
+// resident on device `dev`, so that each CTA fetches the line of the CTA that will replace it), or 0.
+int rc_prefetch_ahead(int n, int u, int dev);
 cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_lines, cudaStream_t s);
 
 // ----------------------------------------------------------- range-Doppler

@@ -13,13 +13,14 @@ import bench  # noqa: E402
 
 
 @pytest.mark.parametrize("nr,u,name", [
-    (512, 8, "rc_reg_kernel<512>"), (4096, 8, "rc_reg_kernel<4096>"), (8192, 1, "rc_reg_kernel<8192>"),
+    (512, 8, "rc_reg_kernel<512>"), (4096, 8, "rc_reg_kernel<4096>"), (8192, 1, "rc_reg32_kernel"), (8192, 8, "rc_reg_kernel<8192>"),
     (6000, 1, "rc_mixed6000_kernel"), (3000, 1, "rc_fused_kernel"), (1200, 8, "rc_fused_kernel"),
     (4094, 1, "rc_blue_reg_kernel<8192>"), (1009, 1, "rc_blue_reg_kernel<2048>"), (257, 1, "rc_blue_reg_kernel<1024>"),
     (100, 1, "rc_fused_kernel"), (17, 1, "rc_blue_reg_kernel<512>"), (4095, 4, "rc_bluestein_kernel"),
 ])
 def test_rc_kernel_name(nr, u, name):
-    # powers of two 512..8192 -> register kernel; 6000 -> its own kernel; other even 2^a 3^b 5^c ->
+    # powers of two 512..8192 -> register kernel (8192 without upsampling: the 32-element one);
+    # 6000 -> its own kernel; other even 2^a 3^b 5^c ->
     # the mixed-radix shared-memory kernel; anything else -> Bluestein with M >= 2 Nr - 1 (at least 512)
     assert bench.rc_kernel_name(nr, u) == name
 

@@ -26,9 +26,9 @@ def _lines(n, lines, seed):
 
 
 def test_wait_that_runs_out_reports_timeout_and_context_survives(monkeypatch):
-    # 8192-sample lines are staged by bulk copy; with the limit at 0 every CTA finds its first copy
-    # still in flight, sets the timeout flag, lets the copy land and returns
-    radar = synth.Radar(range_start=5000.0, n_pulses=64, n_range=8192, upsample=1)
+    # 8192-sample lines with upsampling are staged by bulk copy; with the limit at 0 every CTA finds
+    # its first copy still in flight, sets the timeout flag, lets the copy land and returns
+    radar = synth.Radar(range_start=5000.0, n_pulses=64, n_range=8192, upsample=2)
     raw = _lines(8192, 64, 1)
     monkeypatch.setenv("SAR_WAIT_LIMIT_NS", "0")
     plan = sar.sar_plan_create(radar, None, 0)

@@ -50,6 +50,23 @@ def test_noalloc_matches_form_image_on_two_calls_in_a_row():
         assert rel_l2(g, w) <= IMG_TOL
 
 
+def test_noalloc_records_both_kernel_timings():
+    """With kernel timing on, one call records one range-compression and one backprojection pair,
+    like sar_form_image."""
+    noalloc = _entry()
+    scene = synth.make_scene(1, device="cuda")
+    plan = sar.sar_plan_create(scene["radar"], scene["grid"], 0)
+    sar.sar_plan_set_timing(plan, True)
+    got = torch.empty(scene["grid"].ny, scene["grid"].nx, dtype=torch.complex64, device="cuda")
+    st = noalloc(plan.handle, P(scene["raw"].data_ptr()), P(scene["pos"].data_ptr()), P(got.data_ptr()),
+                 P(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, sar.sar_status_string(st)
+    sar.sar_plan_sync(plan)
+    times = sar.sar_plan_kernel_times(plan)
+    assert times["rc_calls"] == 1 and times["bp_calls"] == 1, times
+    assert times["rc_ms"] > 0 and times["bp_ms"] > 0, times
+
+
 def test_noalloc_rejects_plans_beyond_its_scratch():
     noalloc = _entry()
     s = synth.make_scene(1, device="cuda")
