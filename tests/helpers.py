@@ -10,6 +10,9 @@ ORACLE_THREADS = int(os.environ.get("SAR_ORACLE_THREADS", "0"))   # 0 = all core
 RC_TOL = 2e-4       # relative L2, range compression
 IMG_TOL = 1e-3      # relative L2, image
 PEAK_DB_TOL = 0.05  # peak magnitude, dB
+SNR_DB_TOL = 0.05   # per-target peak-to-background ratio, dB
+SNR_HALF = 10       # SNR window: (2 SNR_HALF + 1)^2 pixels centred on the target's pixel
+SNR_LOBE = 3        # main lobe excluded from the background: pixels within this Chebyshev distance of the peak
 
 
 def rel_l2(got, ref):
@@ -75,3 +78,31 @@ def target_pixels(scene):
     ix = np.rint((xyz[:, 0] - g.x0) / g.dx).astype(int)
     iy = np.rint((xyz[:, 1] - g.y0) / g.dy).astype(int)
     return list(zip(ix.tolist(), iy.tolist()))
+
+
+def target_snr_db(img, grid, centre, half=SNR_HALF, lobe=SNR_LOBE, peak_at=None):
+    """Peak-to-background ratio (dB) of one point target: the largest magnitude in the window of
+    half-width `half` around `centre`, over the RMS magnitude of the window's pixels farther than
+    `lobe` pixels (Chebyshev distance) from the peak (the main lobe excluded).  `peak_at` fixes the
+    peak pixel (window coordinates) instead of searching for it.  Returns (snr_db, peak_index)."""
+    ix, iy = centre
+    y0, y1 = max(0, iy - half), min(grid.ny, iy + half + 1)
+    x0, x1 = max(0, ix - half), min(grid.nx, ix + half + 1)
+    a = np.abs(np.asarray(img)[y0:y1, x0:x1])
+    py, px = np.unravel_index(int(np.argmax(a)), a.shape) if peak_at is None else peak_at
+    yy, xx = np.mgrid[0:a.shape[0], 0:a.shape[1]]
+    bg = a[np.maximum(np.abs(yy - py), np.abs(xx - px)) > lobe]
+    return 20.0 * np.log10(a[py, px] / np.sqrt(np.mean(bg ** 2))), (py, px)
+
+
+def check_snr(img_gpu, img_ref, grid, centres):
+    """Per point target, the GPU image's peak-to-background ratio must match the oracle's within
+    SNR_DB_TOL dB (both measured around the oracle's peak pixel).  Returns the largest difference."""
+    worst = 0.0
+    for c in centres:
+        ref_db, peak = target_snr_db(img_ref, grid, c)
+        got_db, _ = target_snr_db(img_gpu, grid, c, peak_at=peak)
+        d = abs(got_db - ref_db)
+        worst = max(worst, d)
+        assert d <= SNR_DB_TOL, f"target {c}: SNR {got_db:.4f} dB vs oracle {ref_db:.4f} dB"
+    return worst

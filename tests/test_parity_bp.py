@@ -1,7 +1,8 @@
 """GPU backprojection and end-to-end image formation (through the C ABI)
-against the fp64 oracle: relative L2 <= 1e-3 over the image (or over sampled
-pixels at the two large sizes), identical point-target peak pixels and peak
-magnitudes within 0.05 dB."""
+against the fp64 oracle: relative L2 <= 1e-3 over the whole image (over
+sampled pixels and every target's window on the large curved-track scene),
+identical point-target peak pixels, peak magnitudes within 0.05 dB and
+per-target peak-to-background ratios within 0.05 dB."""
 import ctypes
 import dataclasses
 import os
@@ -13,8 +14,8 @@ import torch
 import domain_backprojection_gb300 as sar
 import oracle
 import synth
-from helpers import (IMG_TOL, ORACLE_THREADS, check_peaks, oracle_image_pixels, rel_l2, target_pixels,
-                     window_pixels)
+from helpers import (IMG_TOL, ORACLE_THREADS, SNR_HALF, check_peaks, check_snr, oracle_image_pixels, rel_l2,
+                     target_pixels, window_pixels)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +41,7 @@ def test_form_image_full(scenes, cfg):
     got = img.cpu().numpy()
     assert rel_l2(got, ref) <= IMG_TOL
     check_peaks(got, ref, s["grid"], target_pixels(s), 6)
+    check_snr(got, ref, s["grid"], target_pixels(s))
     # backprojection alone from the oracle's own compressed lines (rounded to complex64)
     img2 = sar.sar_backproject(plan, torch.from_numpy(rc.astype(np.complex64)).cuda(), s["pos"])
     sar.sar_plan_sync(plan)
@@ -48,18 +50,36 @@ def test_form_image_full(scenes, cfg):
     assert rel_l2(img2.cpu().numpy(), ref2) <= IMG_TOL
 
 
-@pytest.mark.parametrize("cfg,n_random", [(3, 4096), (4, 1024)])
-def test_form_image_full_size_sampled(scenes, cfg, n_random):
-    s = scenes(cfg)
+def test_form_image_spotlight_whole(scenes):
+    # the spotlight scene (4096 pulses, 1024 x 1024 pixels): every pixel against the oracle
+    s = scenes(3)
     grid = s["grid"]
     plan = sar.sar_plan_create(s["radar"], grid, 0)
     img = sar.sar_form_image(plan, s["raw"], s["pos"])
     sar.sar_plan_sync(plan)
     got = img.cpu().numpy()
-    rng = np.random.default_rng(cfg)
-    rand = rng.choice(grid.nx * grid.ny, n_random, replace=False)
+    pix = np.arange(grid.nx * grid.ny, dtype=np.int64)
+    ref = oracle_image_pixels(s["radar"], grid, s["raw"].cpu().numpy(), s["pos"].cpu().numpy(), pix)
+    ref = ref.reshape(grid.ny, grid.nx)
+    assert rel_l2(got, ref) <= IMG_TOL
     tp = target_pixels(s)
-    win = window_pixels(grid, tp, 6)
+    check_peaks(got, ref, grid, tp, 6)
+    check_snr(got, ref, grid, tp)
+
+
+def test_form_image_curved_track_sampled(scenes):
+    # the large curved-track scene (16384 pulses, 2048 x 2048 pixels): 1024 random pixels and the
+    # whole window around every target
+    s = scenes(4)
+    grid = s["grid"]
+    plan = sar.sar_plan_create(s["radar"], grid, 0)
+    img = sar.sar_form_image(plan, s["raw"], s["pos"])
+    sar.sar_plan_sync(plan)
+    got = img.cpu().numpy()
+    rng = np.random.default_rng(4)
+    rand = rng.choice(grid.nx * grid.ny, 1024, replace=False)
+    tp = target_pixels(s)
+    win = window_pixels(grid, tp, SNR_HALF)
     pix = np.unique(np.concatenate([rand, win]))
     ref = oracle_image_pixels(s["radar"], grid, s["raw"].cpu().numpy(), s["pos"].cpu().numpy(), pix)
     assert rel_l2(got.ravel()[pix], ref) <= IMG_TOL
@@ -67,7 +87,9 @@ def test_form_image_full_size_sampled(scenes, cfg, n_random):
     assert rel_l2(got.ravel()[pix[in_rand]], ref[in_rand]) <= IMG_TOL
     full_ref = np.zeros(grid.nx * grid.ny, complex)
     full_ref[pix] = ref
-    check_peaks(got, full_ref.reshape(grid.ny, grid.nx), grid, tp, 6)
+    full_ref = full_ref.reshape(grid.ny, grid.nx)
+    check_peaks(got, full_ref, grid, tp, 6)
+    check_snr(got, full_ref, grid, tp)
 
 
 def _small_case(nx=45, ny=70, na=96):
