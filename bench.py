@@ -121,11 +121,13 @@ class ClockSampler:
 
 
 KERNEL_SOURCES = {
-    "bp_kernel": ["bp_kernel.cu", "sar_internal.cuh"],
+    # the pixel kernel's launch shape (tile shape, pulse slices) is chosen in sar_api.cu
+    "bp_kernel": ["bp_kernel.cu", "sar_internal.cuh", "sar_api.cu"],
     "rc_reg_kernel": ["rc_kernel.cu", "fft_reg.cuh", "sar_internal.cuh"],
     "rc_fused_kernel": ["rc_kernel.cu", "fft_reg.cuh", "sar_internal.cuh"],
     "rc_mixed6000_kernel": ["rc_kernel.cu", "fft_reg.cuh", "sar_internal.cuh"],
     "rc_reg32_kernel": ["rc_kernel.cu", "fft_reg.cuh", "sar_internal.cuh"],
+    "rc_blue32_kernel": ["rc_kernel.cu", "fft_reg.cuh", "sar_internal.cuh"],
 }
 
 
@@ -276,6 +278,28 @@ def headline_record(t, scene, cid, args, world, dev, peaks, peak_src, fp32_sm_mh
     }
 
 
+def write_traffic_record(csv_path, kernel, launch, workload, command):
+    """profiles/<kernel>_traffic.json from an ncu --csv log of one launch of `kernel` with
+    dram__bytes_read.sum and dram__bytes_write.sum, tied to the sha256 of the kernel's sources."""
+    import csv
+    rows = [r for r in csv.reader(open(csv_path)) if r and not r[0].startswith("==")]
+    hdr = rows[0]
+    ki, mn, mv, mu = (hdr.index(k) for k in ("Kernel Name", "Metric Name", "Metric Value", "Metric Unit"))
+    vals = {}
+    for r in rows[1:]:
+        if kernel in r[ki]:
+            scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(r[mu], 1)
+            vals[r[mn]] = int(round(float(r[mv].replace(",", "")) * scale))
+    rd, wr = vals["dram__bytes_read.sum"], vals["dram__bytes_write.sum"]
+    rec = {"kernel": kernel, "launch": launch, "workload": workload, "dram_bytes_read": rd,
+           "dram_bytes_write": wr, "dram_bytes_per_launch": rd + wr, "command": command,
+           "source_sha256": source_digest(kernel), "source_files": KERNEL_SOURCES[kernel]}
+    with open(os.path.join(ROOT, "profiles", f"{kernel}_traffic.json"), "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import domain_backprojection_gb300 as sar
@@ -351,6 +375,8 @@ def rc_kernel_name(nr, upsample=1):
     bm = 512
     while bm < 2 * nr - 1:
         bm *= 2
+    if bm == 16384:
+        return "rc_blue32_kernel"
     return f"rc_blue_reg_kernel<{bm}>" if upsample == 1 else "rc_bluestein_kernel"
 
 
@@ -552,9 +578,9 @@ def rc_sweep(dev, peaks, reps=20, n_sets=4, cpu=True, cpu_full=False):
 
     res = {}
     hbm = float(peaks.get("hbm_gbs", 6800.0))
-    # the range-only lengths, then one length with a prime factor (2 x 23 x 89) that takes the
-    # Bluestein kernel
-    for nr in tuple(synth.RC_SWEEP_NR) + (4094,):
+    # the range-only lengths, then two lengths with a prime factor that take the Bluestein kernels
+    # (2 x 23 x 89: M = 8192; 2 x 3^2 x 5 x 7 x 13: M = 16384)
+    for nr in tuple(synth.RC_SWEEP_NR) + (4094, 8190):
         scene = synth.make_rc_sweep(nr, n_lines=4096, device=dev)
         plan = sar.sar_plan_create(scene["radar"], None, dev.index)
         raws = [scene["raw"]] + [scene["raw"].clone() for _ in range(n_sets - 1)]
@@ -756,8 +782,14 @@ def main():
                          "the same on the tiny, small and large curved-track scenes; 'sweepNR' (e.g. NR = 4096, 8192, "
                          "6000, 4094) range-compresses the 4096 lines of the range-only workload three times; 'rda' forms "
                          "two range-Doppler images of the spotlight scene's raw echoes")
+    ap.add_argument("--write-traffic", nargs=5, metavar=("CSV", "KERNEL", "LAUNCH", "WORKLOAD", "COMMAND"),
+                    help="write profiles/KERNEL_traffic.json from an ncu --csv log of one launch (DRAM bytes read "
+                         "and written) and exit")
     args = ap.parse_args()
     rank, world, local_rank = rank_env()
+    if args.write_traffic:
+        print(json.dumps(write_traffic_record(*args.write_traffic)))
+        return
     if args.profile_case:
         profile_case(args.profile_case)
         return

@@ -336,27 +336,20 @@ __device__ __forceinline__ float df_floor(dflt x, float &frac)
     return fl;
 }
 
-// Antenna positions, float64 [n][3] -> double-float [n][3] (hi, lo) pairs.
-__global__ void __launch_bounds__(256) bp_split_pos_kernel(const double *pos, float2 *out, int begin, int end)
+// A float64 value as a double-float (hi, lo) pair.
+__device__ __forceinline__ dflt df_from_double(double v)
 {
-    const int n = begin + blockIdx.x * blockDim.x + threadIdx.x;
-    if (n >= end) return;
-#pragma unroll
-    for (int k = 0; k < 3; k++) {
-        const double v = pos[3 * n + k];
-        const float hi = (float)v;
-        out[3 * n + k] = make_float2(hi, (float)(v - (double)hi));
-    }
+    const float hi = (float)v;
+    return {hi, (float)(v - (double)hi)};
 }
 
 // Per (tile, pulse) reference range (double-float) and window extent (float32), one thread each.
 // Output: pa = (a, b, c, q0m), pc = (c1, c2, c3, theta), win = (origin o, first entry, last entry, 0).
-__device__ __forceinline__ void tile_pulse_params(const BpArgs &args, int tile_x, int tile_y, int n, float4 &pa,
-                                                  float4 &pc, int4 &win)
+// (ax, ay, az): the pulse's antenna position in double-float.
+__device__ __forceinline__ void tile_pulse_params(const BpArgs &args, int tile_x, int tile_y, const dflt ax,
+                                                  const dflt ay, const dflt az, float4 &pa, float4 &pc, int4 &win)
 {
     const int w = args.w, wh = args.wh;
-    const float2 *ap = args.pos_split + 3 * n;
-    const dflt ax = {ap[0].x, ap[0].y}, ay = {ap[1].x, ap[1].y}, az = {ap[2].x, ap[2].y};
     // tile centre: x0 + (tile * 64 + 31.5) dx, y0 + (tile * 32 + 15.5) dy (the float multipliers are exact)
     const dflt cx = df_add({args.x0s.x, args.x0s.y},
                            df_mulf({args.dxs.x, args.dxs.y}, (float)tile_x * args.tile_w + 0.5f * (args.tile_w - 1)));
@@ -411,20 +404,32 @@ __device__ __forceinline__ void tile_pulse_params(const BpArgs &args, int tile_x
 }
 
 // The parameter table: entry (tile, pulse) at table + 3 (tile_index * pulse_count + pulse - pulse_begin).
+// One thread per pulse and group of kBpPrepTiles consecutive tiles (pulses fastest, so that a
+// warp's writes of one tile's entries are contiguous): the pulse's float64 position is split into
+// double-float once per group (float64 runs at a small fraction of the float32 rate here).
+constexpr int kBpPrepTiles = 16;
+
 __global__ void __launch_bounds__(256) bp_prep_kernel(BpArgs args)
 {
     const int64_t npulses = args.pulse_end - args.pulse_begin;
-    const int64_t total = npulses * args.tiles_x * args.tiles_y;
+    const int tiles = args.tiles_x * args.tiles_y;
+    const int groups = (tiles + kBpPrepTiles - 1) / kBpPrepTiles;
+    const int64_t total = npulses * groups;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t tile = i / npulses;
-        const int n = args.pulse_begin + (int)(i - tile * npulses);
-        float4 pa, pc;
-        int4 win;
-        tile_pulse_params(args, (int)(tile % args.tiles_x), (int)(tile / args.tiles_x), n, pa, pc, win);
-        float4 *dst = args.table + 3 * i;
-        dst[0] = pa;
-        dst[1] = pc;
-        dst[2] = make_float4(__int_as_float(win.x), __int_as_float(win.y), __int_as_float(win.z), 0.0f);
+        const int group = (int)(i / npulses);
+        const int64_t pi = i - (int64_t)group * npulses;
+        const double *ap = args.pos + 3 * (args.pulse_begin + pi);
+        const dflt ax = df_from_double(__ldg(ap)), ay = df_from_double(__ldg(ap + 1)), az = df_from_double(__ldg(ap + 2));
+        const int t_end = min(tiles, (group + 1) * kBpPrepTiles);
+        for (int tile = group * kBpPrepTiles; tile < t_end; tile++) {
+            float4 pa, pc;
+            int4 win;
+            tile_pulse_params(args, tile % args.tiles_x, tile / args.tiles_x, ax, ay, az, pa, pc, win);
+            float4 *dst = args.table + 3 * ((int64_t)tile * npulses + pi);
+            dst[0] = pa;
+            dst[1] = pc;
+            dst[2] = make_float4(__int_as_float(win.x), __int_as_float(win.y), __int_as_float(win.z), 0.0f);
+        }
     }
 }
 
@@ -787,9 +792,8 @@ cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream
 {
     if (a.pulse_end <= a.pulse_begin) return cudaSuccess;
     const int npulse = a.pulse_end - a.pulse_begin;
-    bp_split_pos_kernel<<<(npulse + 255) / 256, 256, 0, s>>>(a.pos, a.pos_split, a.pulse_begin, a.pulse_end);
-    const int64_t entries = (int64_t)npulse * a.tiles_x * a.tiles_y;
-    const int64_t prep_blocks = (entries + 255) / 256;
+    const int64_t groups = (a.tiles_x * a.tiles_y + kBpPrepTiles - 1) / kBpPrepTiles;
+    const int64_t prep_blocks = ((int64_t)npulse * groups + 255) / 256;
     bp_prep_kernel<<<(unsigned)(prep_blocks < (1 << 20) ? prep_blocks : (1 << 20)), 256, 0, s>>>(a);
     cudaError_t pe = cudaGetLastError();
     if (pe != cudaSuccess) return pe;

@@ -24,7 +24,8 @@
 //   - rc_fused_kernel: other even 2^a 3^b 5^c lengths, mixed-radix Stockham passes
 //     (16, 8, 5, 4, 3, 2) between two shared-memory buffers, the spectrum in a third;
 //   - rc_blue_reg_kernel<M> (U = 1) and rc_bluestein_kernel (U > 1): any other
-//     length up to 4096, as Bluestein transforms of a power-of-two length M.
+//     length up to 4096, as Bluestein transforms of a power-of-two length M;
+//     rc_blue32_kernel: any other length from 4097 to 8192 (M = 16384).
 #include "fft_reg.cuh"
 
 namespace sar {
@@ -671,6 +672,118 @@ __global__ void __launch_bounds__(M / 16, rc_blue_min_ctas<M>())
 template <int M>
 size_t rc_blue_reg_smem() { return (size_t)(M + M / 16) * sizeof(float2); }
 
+// Bluestein lines of 4097 .. 8192 samples, both without and with upsampling (convolution length
+// M = 16384): 512 threads of 32 elements, element t + T p in slot p (T = 512), M-point transforms
+// of radix 32, 16 and 32 with two exchanges through one padded buffer (135 KB, one CTA per SM).
+// Without upsampling four transforms per line, as in rc_blue_reg_kernel.  With upsampling the
+// filtered spectrum Y waits in shared memory (each thread reads back only its own bins) and every
+// polyphase component u runs one forward Bluestein transform of conj(Y) exp(-j 2 pi k_s u / (U Nr)),
+// as in rc_bluestein_kernel.
+constexpr int kBlue32M = 16384, kBlue32Threads = 512, kBlue32Elems = 32;
+
+__host__ __device__ constexpr size_t rc_blue32_smem(bool multi)
+{
+    return (size_t)(kBlue32M + kBlue32M / 32) * sizeof(float2) + (multi ? (size_t)8192 * sizeof(float2) : 0);
+}
+
+// forward M-point DFT of the elements held as x[p] = element t + T p; result in the same layout
+__device__ __forceinline__ void blue32_dft(float2 (&x)[kBlue32Elems], float2 *buf, const float2 *__restrict__ tw)
+{
+    constexpr int M = kBlue32M, E = kBlue32Elems;
+    mixed_pass<M, E, 32, 1, true, false, true, true>(x, nullptr, buf, tw);
+    mixed_pass<M, E, 16, 32, false, false, true, true>(x, buf, buf, tw);
+    mixed_pass<M, E, 32, 512, false, true, true, true>(x, buf, nullptr, tw);
+    __syncthreads();                                            // the buffer is free for the next transform
+}
+
+// x <- conj(x Bf): the convolution with the chirp, ready for the transform that inverts it
+__device__ __forceinline__ void blue32_filter(float2 (&x)[kBlue32Elems], const RcArgs &args)
+{
+#pragma unroll
+    for (int p = 0; p < kBlue32Elems; p++) x[p] = cconj(cmul(x[p], __ldg(args.bf + threadIdx.x + kBlue32Threads * p)));
+}
+
+template <bool kMulti>
+__global__ void __launch_bounds__(kBlue32Threads, 1)
+    rc_blue32_kernel(const float2 *__restrict__ raw, float2 *__restrict__ rc, int64_t n_lines, RcArgs args)
+{
+    constexpr int T = kBlue32Threads, E = kBlue32Elems;
+    extern __shared__ float4 smem4[];
+    float2 *buf = reinterpret_cast<float2 *>(smem4);
+    float2 *ysm = buf + kBlue32M + kBlue32M / 32;              // [Nr] filtered spectrum (with upsampling)
+    const int t = threadIdx.x, n = args.n;
+    const int U = kMulti ? args.u : 1, un = U * n;
+    const int lo_mask = (1 << args.ptw_lo_bits) - 1;
+    // z_u = conj(Y) exp(-j 2 pi k_s u / (U Nr)) bw, the input of component u's forward transform
+    auto component_input = [&](float2 (&x)[E], int u) {
+#pragma unroll
+        for (int p = 0; p < E; p++) {
+            const int k = t + T * p;
+            float2 z = make_float2(0.0f, 0.0f);
+            if (k < n) {
+                z = cconj(ysm[k]);
+                if (u != 0) {
+                    const int ks = (2 * k >= n) ? k - n : k;
+                    int tt = (ks * u) % un;
+                    if (tt < 0) tt += un;
+                    z = cmul(z, cmul(__ldg(args.ptw_hi + (tt >> args.ptw_lo_bits)), __ldg(args.ptw_lo + (tt & lo_mask))));
+                }
+                z = cmul(z, __ldg(args.bw + k));
+            }
+            x[p] = z;
+        }
+    };
+    for (int64_t line = blockIdx.x; line < n_lines; line += gridDim.x) {
+        const float2 *src = raw + line * n;
+        float2 *out = rc + line * (int64_t)un;
+        float2 x[E];
+#pragma unroll
+        for (int p = 0; p < E; p++) {
+            const int k = t + T * p;
+            x[p] = k < n ? cmul(__ldg(src + k), __ldg(args.bw + k)) : make_float2(0.0f, 0.0f);
+        }
+        // one copy of the transform code: every Bluestein transform is two M-point transforms with
+        // the chirp filter between them (even trips); after the odd trips the line's spectrum is
+        // filtered (trip 1), or a result is stored (later odd trips)
+        const int trips = kMulti ? 2 + 2 * U : 4;
+#pragma unroll 1
+        for (int trip = 0; trip < trips; trip++) {
+            blue32_dft(x, buf, args.btw);
+            if ((trip & 1) == 0) {
+                blue32_filter(x, args);
+            } else if (trip == 1) {
+                // X[k] = bw[k] conj(x[k]); Y = X H
+#pragma unroll
+                for (int p = 0; p < E; p++) {
+                    const int k = t + T * p;
+                    if (k < n) {
+                        const float2 w = __ldg(args.bw + k);
+                        const float2 y = cmul(cmul(w, cconj(x[p])), __ldg(args.h + k));
+                        if constexpr (kMulti) ysm[k] = y;
+                        else x[p] = cmul(cconj(y), w);              // conj(Y) bw: the inverse transform's input
+                    } else {
+                        x[p] = make_float2(0.0f, 0.0f);
+                    }
+                }
+                if constexpr (kMulti) component_input(x, 0);
+            } else {
+                // a finished inverse transform: sample U m + u = conj(bw conj(x)) = x conj(bw)
+                const int u = kMulti ? (trip - 3) / 2 : 0;
+#pragma unroll
+                for (int p = 0; p < E; p++) {
+                    const int k = t + T * p;
+                    if (k < n) {
+                        const float2 v = cmul(x[p], cconj(__ldg(args.bw + k)));
+                        if (!kMulti || args.planar) out[(int64_t)u * n + k] = v;
+                        else out[(int64_t)U * k + u] = v;
+                    }
+                }
+                if (kMulti && u + 1 < U) component_input(x, u + 1);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 int rc_block_threads(int n) { return n >= 4096 ? 512 : 256; }
@@ -734,6 +847,12 @@ cudaError_t rc_configure(int)
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(rc_reg32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rc8192_smem());
     if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_blue32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rc_blue32_smem(false));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_blue32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rc_blue32_smem(true));
+    if (e == cudaSuccess)
         e = cudaFuncSetAttribute(rc_mixed6000_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)rc_mixed_smem(false));
     if (e == cudaSuccess)
@@ -794,7 +913,10 @@ cudaError_t launch_rc(const RcArgs &a, const float2 *raw, float2 *rc, int64_t n_
         else rc_mixed6000_kernel<true><<<grid, 200, rc_mixed_smem(true), s>>>(raw, rc, n_lines, a);
         break;
     default:
-        if (a.bm > 0 && a.u == 1) {
+        if (a.bm == kBlue32M) {
+            if (a.u == 1) rc_blue32_kernel<false><<<grid, kBlue32Threads, rc_blue32_smem(false), s>>>(raw, rc, n_lines, a);
+            else rc_blue32_kernel<true><<<grid, kBlue32Threads, rc_blue32_smem(true), s>>>(raw, rc, n_lines, a);
+        } else if (a.bm > 0 && a.u == 1) {
             switch (a.bm) {
             case 512: rc_blue_reg_kernel<512><<<grid, 32, rc_blue_reg_smem<512>(), s>>>(raw, rc, n_lines, a); break;
             case 1024: rc_blue_reg_kernel<1024><<<grid, 64, rc_blue_reg_smem<1024>(), s>>>(raw, rc, n_lines, a); break;

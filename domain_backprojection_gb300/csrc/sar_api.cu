@@ -31,7 +31,6 @@ struct sar_plan_s {
     int bp_max_slices = 1;            // pulse slices the partial-image buffer can hold
     float2 *d_partial = nullptr;      // [bp_max_slices][ny][nx] partial images
     float4 *d_table = nullptr;        // [tiles][n_pulses] x 48 B per-(tile, pulse) parameters
-    float2 *d_pos_split = nullptr;    // [n_pulses][3] double-float antenna positions
     // range-Doppler (sar_plan_set_range_doppler): azimuth twiddles | phase coefficients | migration factors
     sar::RdaArgs rd{};
     void *d_rd_tables = nullptr;
@@ -132,9 +131,9 @@ int plan_radices(int n, int *radix)
 }
 
 // Lines the mixed-radix kernels transform directly: even, 2^a 3^b 5^c, up to 8192 samples.  Other
-// lengths from 16 to 4096 go through Bluestein transforms of length M <= 8192.
+// lengths from 16 to 8192 go through Bluestein transforms of length M <= 16384.
 bool direct_length(int n) { return n >= 16 && n <= 8192 && (n & 1) == 0 && factor_235(n); }
-bool bluestein_length(int n) { return !direct_length(n) && n >= 16 && n <= 4096; }
+bool bluestein_length(int n) { return !direct_length(n) && n >= 16 && n <= 8192; }
 
 // In-place radix-2 DFT of length m (a power of two), sign -1, float64 (host tables only).
 void host_fft(std::vector<double> &re, std::vector<double> &im)
@@ -471,10 +470,8 @@ sar_status setup_bp(sar_plan p)
     {
         const size_t entries = (size_t)a.tiles_x * a.tiles_y * r.n_pulses;
         cudaError_t et = dev_alloc(&p->d_table, entries * 3 * sizeof(float4));
-        if (et == cudaSuccess) et = dev_alloc(&p->d_pos_split, (size_t)r.n_pulses * 3 * sizeof(float2));
         if (et != cudaSuccess) return cuda_status(et);
         a.table = p->d_table;
-        a.pos_split = p->d_pos_split;
     }
     const int smem = (int)sar::bp_smem_bytes(a);
     cudaError_t e = sar::bp_configure(smem);
@@ -539,7 +536,6 @@ void free_plan(sar_plan p)
     cudaFree(p->d_tables);
     cudaFree(p->d_partial);
     cudaFree(p->d_table);
-    cudaFree(p->d_pos_split);
     cudaFree(p->d_rd_tables);
     cudaFree(p->d_blue);
     cudaFree(p->d_err);
@@ -580,7 +576,7 @@ sar_status do_backproject(sar_plan plan, const void *rc, const double *pos, int3
         a.table += (size_t)3 * a.tiles_x * a.tiles_y * pulse_begin;
         if (partial) a.partial = partial;
     }
-    plan->last_launches += slices > 1 ? 4 : 3;
+    plan->last_launches += slices > 1 ? 3 : 2;
     const auto ev = timing_pair(plan, plan->ev_bp);
     return cuda_status(sar::launch_bp(a, slices, plan->check_bounds, s, ev.first, ev.second, image_wait, image_done));
 }

@@ -127,9 +127,8 @@ struct BpArgs {
     float2 *partial;
     // per (tile, pulse) parameters written by the prep kernel: 3 float4 per entry
     float4 *table;
-    // double-float (hi, lo) copies of the float64 constants the prep kernel needs, and of the positions
+    // double-float (hi, lo) copies of the float64 constants the prep kernel needs
     float2 x0s, y0s, z0s, dxs, dys, rss, idrs, ph0s, kps;
-    float2 *pos_split;       // [Na][3]
     // data
     const float2 *rc;        // [Na][U Nr], natural order or polyphase planes (planar != 0)
     int planar, u_shift, u_mask, n_range;   // planes: sample I of a line at (I & u_mask) Nr + (I >> u_shift)

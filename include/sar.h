@@ -60,9 +60,9 @@ typedef struct {
     double range_start;   /* slant range of sample 0, m */
     int32_t n_pulses;     /* pulses Na (>= 1) */
     int32_t n_range;      /* samples per pulse Nr: 16 <= Nr <= 8192 when even and of the form
-                             2^a 3^b 5^c (mixed-radix transforms); any other 16 <= Nr <= 4096
-                             (Bluestein / chirp-z transforms, "Ultra-high-resolution airborne
-                             SAR on CUDA", section 5.1) */
+                             2^a 3^b 5^c (mixed-radix transforms); any other 16 <= Nr <= 8192
+                             (Bluestein / chirp-z transforms of length up to 16384,
+                             "Ultra-high-resolution airborne SAR on CUDA", section 5.1) */
     int32_t upsample;     /* range upsampling U in {1, 2, 4, 8} */
 } sar_radar;
 
@@ -302,7 +302,7 @@ sar_status sar_range_doppler(sar_plan plan, const void *raw, void *image, void *
 /* Kernel timing, for benchmarks (no counterpart in the pages).  With enable != 0,
  * each later range-compression call records a pair of CUDA events on its stream
  * around the transform kernel, and each backprojection around the pixel kernel
- * alone (not its small position-split, prep and reduction launches); at most
+ * alone (not its small per-tile parameter and slice-sum launches); at most
  * 4096 calls of each kind are recorded until the next read.  The events belong
  * to the plan.  enable = 0 stops recording.  Errors: SAR_ERR_INVALID_ARG for a
  * NULL plan. */

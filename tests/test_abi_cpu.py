@@ -73,9 +73,9 @@ def test_null_handles():
 @pytest.mark.parametrize("change,expect", [
     (dict(fs=-1.0), 1), (dict(fc=math.nan), 1), (dict(range_start=math.inf), 1), (dict(bandwidth=0.0), 1),
     (dict(n_pulses=0), 1), (dict(upsample=0), 1),
-    (dict(n_range=8190), 2),        # 2 * 3^2 * 5 * 7 * 13: beyond the Bluestein limit (4096)
-    (dict(n_range=4098), 2),        # 2 * 3 * 683: beyond the Bluestein limit
-    (dict(n_range=4097), 2),        # odd, beyond the Bluestein limit
+    (dict(n_range=8193), 2),        # odd, beyond the Bluestein limit (8192)
+    (dict(n_range=8194), 2),        # 2 * 17 * 241: beyond the Bluestein limit
+    (dict(n_range=10000), 2),       # 2^4 5^4, but beyond the on-chip line
     (dict(n_range=16384), 2),       # beyond the on-chip line
     (dict(n_range=15), 2),          # below 16
     (dict(upsample=3), 2), (dict(upsample=16), 2),

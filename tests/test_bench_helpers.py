@@ -17,6 +17,7 @@ import bench  # noqa: E402
     (6000, 1, "rc_mixed6000_kernel"), (3000, 1, "rc_fused_kernel"), (1200, 8, "rc_fused_kernel"),
     (4094, 1, "rc_blue_reg_kernel<8192>"), (1009, 1, "rc_blue_reg_kernel<2048>"), (257, 1, "rc_blue_reg_kernel<1024>"),
     (100, 1, "rc_fused_kernel"), (17, 1, "rc_blue_reg_kernel<512>"), (4095, 4, "rc_bluestein_kernel"),
+    (5003, 1, "rc_blue32_kernel"), (8190, 8, "rc_blue32_kernel"),
 ])
 def test_rc_kernel_name(nr, u, name):
     # powers of two 512..8192 -> register kernel (8192 without upsampling: the 32-element one);
@@ -28,7 +29,7 @@ def test_rc_kernel_name(nr, u, name):
 def test_traffic_record_follows_the_sources(tmp_path, monkeypatch):
     # every committed record names its kernel, carries read + write = per-launch bytes, and is
     # reported only while the sha256 of the kernel's sources matches
-    for kernel in ("bp_kernel", "rc_reg_kernel", "rc_mixed6000_kernel"):
+    for kernel in ("bp_kernel", "rc_reg_kernel", "rc_mixed6000_kernel", "rc_reg32_kernel"):
         with open(os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")) as f:
             rec = json.load(f)
         assert rec["kernel"] == kernel
@@ -39,10 +40,10 @@ def test_traffic_record_follows_the_sources(tmp_path, monkeypatch):
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
     src = os.path.join(ROOT, "domain_backprojection_gb300", "csrc")
-    for name in ("bp_kernel.cu", "sar_internal.cuh"):
+    for name in bench.KERNEL_SOURCES["bp_kernel"]:
         with open(os.path.join(src, name), "rb") as f:
             (csrc / name).write_bytes(f.read())
-    rec = {"kernel": "bp_kernel", "dram_bytes_per_launch": 123, "source_files": ["bp_kernel.cu", "sar_internal.cuh"]}
+    rec = {"kernel": "bp_kernel", "dram_bytes_per_launch": 123, "source_files": bench.KERNEL_SOURCES["bp_kernel"]}
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     rec["source_sha256"] = bench.source_digest("bp_kernel")
     (tmp_path / "profiles" / "bp_kernel_traffic.json").write_text(json.dumps(rec))

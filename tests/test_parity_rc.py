@@ -38,8 +38,10 @@ def _run(radar, raw_cpu):
     (16, 1, 3), (16, 8, 2), (30, 2, 5), (240, 4, 7), (1000, 1, 9), (1000, 8, 3), (1536, 2, 4),
     (1024, 1, 1), (1024, 8, 37), (2048, 8, 64), (4096, 1, 100), (4096, 1, 7), (4096, 1, 1), (4096, 8, 16),
     (6000, 1, 50), (6000, 8, 5), (8192, 1, 33), (8192, 1, 2), (8192, 8, 9), (8192, 4, 3), (4050, 2, 3),
-    # Bluestein lengths: 2 * 3^3 * 19, the prime 1009, odd 3 * 5^3, 2 * 23 * 89, the largest odd
+    # Bluestein lengths: 2 * 3^3 * 19, the prime 1009, odd 3 * 5^3, 2 * 23 * 89, odd 3^2 5 7 13;
+    # beyond 4096 (M = 16384): the prime 5003, the odd 4097 = 17 * 241, 2 * 3^2 * 5 * 7 * 13, and 8191
     (1026, 1, 5), (1026, 8, 3), (1009, 2, 4), (375, 1, 3), (375, 4, 2), (4094, 4, 2), (4095, 1, 2),
+    (5003, 1, 3), (5003, 8, 2), (4097, 2, 2), (8190, 1, 3), (8190, 8, 2), (8191, 4, 2),
 ])
 def test_rc_random_lines(n, U, lines):
     radar = _short_pulse_radar(n, U, lines) if n < 400 else synth.Radar(range_start=5000.0, n_pulses=lines,

@@ -44,7 +44,7 @@ def test_noalloc_matches_form_image_on_two_calls_in_a_row():
                      P(stream.cuda_stream))
         assert st == 0, sar.sar_status_string(st)
         sar.sar_plan_sync(plan)
-        assert 2 <= sar.sar_plan_last_launches(plan) <= 5
+        assert 2 <= sar.sar_plan_last_launches(plan) <= 4
         w, g = want.cpu().numpy(), got.cpu().numpy()
         assert np.all(np.isfinite(g))
         assert rel_l2(g, w) <= IMG_TOL
