@@ -404,24 +404,26 @@ __device__ __forceinline__ void tile_pulse_params(const BpArgs &args, int tile_x
 }
 
 // The parameter table: entry (tile, pulse) at table + 3 (tile_index * pulse_count + pulse - pulse_begin).
-// One thread per pulse and group of kBpPrepTiles consecutive tiles (pulses fastest, so that a
-// warp's writes of one tile's entries are contiguous): the pulse's float64 position is split into
-// double-float once per group (float64 runs at a small fraction of the float32 rate here).
+// One thread per pulse and group of `group` consecutive tiles (pulses fastest, so that a warp's
+// writes of one tile's entries are contiguous): the pulse's float64 position is split into
+// double-float once per group (float64 runs at a small fraction of the float32 rate here).  The
+// launcher makes groups of up to kBpPrepTiles tiles, fewer when that would leave the GPU short of
+// threads (a small image).
 constexpr int kBpPrepTiles = 16;
 
-__global__ void __launch_bounds__(256) bp_prep_kernel(BpArgs args)
+__global__ void __launch_bounds__(256) bp_prep_kernel(BpArgs args, int group)
 {
     const int64_t npulses = args.pulse_end - args.pulse_begin;
     const int tiles = args.tiles_x * args.tiles_y;
-    const int groups = (tiles + kBpPrepTiles - 1) / kBpPrepTiles;
+    const int groups = (tiles + group - 1) / group;
     const int64_t total = npulses * groups;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int group = (int)(i / npulses);
-        const int64_t pi = i - (int64_t)group * npulses;
+        const int g = (int)(i / npulses);
+        const int64_t pi = i - (int64_t)g * npulses;
         const double *ap = args.pos + 3 * (args.pulse_begin + pi);
         const dflt ax = df_from_double(__ldg(ap)), ay = df_from_double(__ldg(ap + 1)), az = df_from_double(__ldg(ap + 2));
-        const int t_end = min(tiles, (group + 1) * kBpPrepTiles);
-        for (int tile = group * kBpPrepTiles; tile < t_end; tile++) {
+        const int t_end = min(tiles, (g + 1) * group);
+        for (int tile = g * group; tile < t_end; tile++) {
             float4 pa, pc;
             int4 win;
             tile_pulse_params(args, tile % args.tiles_x, tile / args.tiles_x, ax, ay, az, pa, pc, win);
@@ -792,9 +794,13 @@ cudaError_t launch_bp(const BpArgs &a, int slices, bool check_bounds, cudaStream
 {
     if (a.pulse_end <= a.pulse_begin) return cudaSuccess;
     const int npulse = a.pulse_end - a.pulse_begin;
-    const int64_t groups = (a.tiles_x * a.tiles_y + kBpPrepTiles - 1) / kBpPrepTiles;
+    const int64_t tiles = (int64_t)a.tiles_x * a.tiles_y;
+    // tiles per thread: up to kBpPrepTiles while that still leaves ~1024 threads per SM
+    const int64_t per_thread = (tiles * npulse + 155647) / 155648;
+    const int group = (int)(per_thread < 1 ? 1 : per_thread > kBpPrepTiles ? kBpPrepTiles : per_thread);
+    const int64_t groups = (tiles + group - 1) / group;
     const int64_t prep_blocks = ((int64_t)npulse * groups + 255) / 256;
-    bp_prep_kernel<<<(unsigned)(prep_blocks < (1 << 20) ? prep_blocks : (1 << 20)), 256, 0, s>>>(a);
+    bp_prep_kernel<<<(unsigned)(prep_blocks < (1 << 20) ? prep_blocks : (1 << 20)), 256, 0, s>>>(a, group);
     cudaError_t pe = cudaGetLastError();
     if (pe != cudaSuccess) return pe;
     const dim3 grid(a.tiles_x, a.tiles_y, slices);
