@@ -512,8 +512,9 @@ def other_scenes(dev, peaks, fp32_peak, reps=20, cpu=True, cpu_full=False):
     """The tiny (256 x 1024, 128^2) and small (1024 x 2048, 512^2) scenes, each formed as the headline
     step forms its image (range compression into polyphase planes, then backprojection).  Per scene:
     step time, pixel-pulse and line rates, the backprojection kernel's fraction of the FP32 peak, the
-    range compression's fraction of the measured HBM bandwidth, and the oracle timed on the whole
-    scene.  Both scenes' inputs fit in L2, so their rates are L2-warm.  (The large curved-track
+    range compression's fraction of the measured HBM bandwidth, the same step replayed from a CUDA
+    graph, and the oracle timed on the whole scene.  Both scenes' inputs fit in L2, so their rates
+    are L2-warm.  (The large curved-track
     scene has a record of its own, in the headline's form.)"""
     import torch
     import domain_backprojection_gb300 as sar
@@ -544,9 +545,32 @@ def other_scenes(dev, peaks, fp32_peak, reps=20, cpu=True, cpu_full=False):
         torch.cuda.synchronize(dev)
         sar.sar_plan_sync(plan)
         kt = sar.sar_plan_kernel_times(plan)
+        sar.sar_plan_set_timing(plan, False)
         step_ms = e0.elapsed_time(e1) / reps
         bp_ms = kt["bp_ms"] / kt["bp_calls"]
         rc_ms = kt["rc_ms"] / kt["rc_calls"]
+        # the same step captured once in a CUDA graph and replayed: the launches without their
+        # host-side gaps (these scenes are small enough for the gaps to show)
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                sar.sar_range_compress(plan, scene["raw"], rc, stream=cap)
+                sar.sar_backproject(plan, rc, scene["pos"], image=img, stream=cap)
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(reps):
+            graph.replay()
+        g1.record()
+        torch.cuda.synchronize(dev)
+        sar.sar_plan_sync(plan)
+        graph_ms = g0.elapsed_time(g1) / reps
+        del graph
         pp = cfg.pixel_pulses
         rc_gbs = cfg.n_pulses * 8 * radar.n_range * (1 + radar.upsample) / (rc_ms * 1e-3) / 1e9
         bp_tflops = FLOPS_PER_PIXEL_PULSE * pp / (bp_ms * 1e-3) / 1e12
@@ -555,6 +579,8 @@ def other_scenes(dev, peaks, fp32_peak, reps=20, cpu=True, cpu_full=False):
                         f"{grid.nx}x{grid.ny} @ {grid.dx} m",
             "pixel_pulses": pp, "step_ms": round(step_ms, 4),
             "step_gpix_pulse_per_s": round(pp / (step_ms * 1e-3) / 1e9, 1),
+            "step_ms_graph": round(graph_ms, 4),
+            "step_graph_gpix_pulse_per_s": round(pp / (graph_ms * 1e-3) / 1e9, 1),
             "bp_kernel_ms": round(bp_ms, 4), "bp_gpix_pulse_per_s": round(pp / (bp_ms * 1e-3) / 1e9, 1),
             "bp_frac_fp32": round(bp_tflops / fp32_peak, 4),
             "rc_kernel": rc_kernel_name(radar.n_range, radar.upsample), "rc_kernel_ms": round(rc_ms, 4),
