@@ -77,3 +77,29 @@ def test_rc_context_flops():
     # 5 N log2 N per transform, (1 + U) transforms, plus the 6 N flops of the filter product
     assert bench.rc_flops_per_line(4096, 8) == 5 * 4096 * 12 * 9 + 6 * 4096
     assert bench.rc_flops_per_line(1024, 1) == 5 * 1024 * 10 * 2 + 6 * 1024
+
+
+def test_oracle_timing_records_on_a_small_case():
+    # the CPU-baseline records: whole-step timing when nothing is sampled, scaled sampling otherwise,
+    # and the range-only record in lines/s; every record names its cores, CPU model and sample
+    import dataclasses
+    import synth
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=32, nx=16, ny=16)
+    scene = synth.make_scene(cfg, device="cpu")
+    whole = bench.oracle_baseline(scene, 1, threads=1)
+    assert whole["kind"] == "oracle" and whole["cores"] == 1 and not whole["extrapolated"]
+    assert whole["value"] > 0 and whole["full_step_s"] > 0 and whole["cpu"]
+    assert whole["sample"].startswith("whole step")
+    pp = 32 * 16 * 16
+    assert abs(whole["value"] - pp / (whole["rc_s"] + whole["bp_s"]) / 1e9) <= 0.02 * whole["value"] + 1e-5
+    # a sampled record (the spotlight rule: first 256 pulses, central 256^2 pixels) extrapolates
+    big = dataclasses.replace(synth.SCENES[1], n_pulses=300, nx=300, ny=300)
+    s2 = synth.make_scene(big, device="cpu")
+    samp = bench.oracle_baseline(s2, 3, threads=1)
+    assert samp["extrapolated"] and "256 of 300" in samp["sample"] and "256x256" in samp["sample"]
+    sweep = synth.make_rc_sweep(1024, n_lines=64, device="cpu")
+    rc = bench.oracle_rc_baseline(sweep, threads=1)
+    assert rc["unit"] == "lines/s" and rc["value"] > 0 and not rc["extrapolated"]
+    rc1 = bench.oracle_rc_baseline(synth.make_rc_sweep(1024, n_lines=1024, device="cpu"), threads=1)
+    assert rc1["extrapolated"] and "512 of 1024" in rc1["sample"]
+    assert bench.central_pixels(cfg.grid(), 4).tolist() == [6 * 16 + 6 + i + 16 * j for j in range(4) for i in range(4)]
