@@ -54,9 +54,10 @@ def test_rc_random_lines(n, U, lines):
         assert rel_l2(got[i], ref[i]) <= RC_TOL, f"line {i}"
 
 
-@pytest.mark.parametrize("nr", synth.RC_SWEEP_NR)
+@pytest.mark.parametrize("nr", tuple(synth.RC_SWEEP_NR) + (4094, 8190))
 def test_rc_sweep_full_size(nr):
-    # the range-compression-only workload at its full size (4096 lines), sampled lines checked
+    # the range-compression-only workload at its full size (4096 lines), sampled lines checked; also
+    # at two Bluestein lengths (convolution lengths 8192 and 16384) in the same launch shape
     scene = synth.make_rc_sweep(nr, n_lines=4096, device="cuda")
     radar = scene["radar"]
     plan = sar.sar_plan_create(radar, None, 0)
