@@ -9,13 +9,13 @@
 // compressed samples a tile touches grows with its range (y) extent only and staging it is shared
 // by more pixels.  Warps run along x, so the 32 lanes of a warp read nearly the same samples; each
 // thread keeps eight pixels' complex sums (one column, eight consecutive rows) in registers for
-// the whole pulse range.  The CTA walks the
-// pulses in batches: for each pulse of a batch it first evaluates, in float64,
-// the range R0 from the antenna to the tile centre, then stages the window of
-// compressed samples the tile can touch in shared memory (section 2.3 of the
-// same page stages echo data per image block the same way).  Long pulse ranges
-// are split into slices (gridDim.z) whose partial images a second kernel adds
-// in slice order, so that small images and the last wave still fill the GPU.
+// the whole pulse range.  A prep kernel first evaluates, per (tile, pulse) and in double-float
+// arithmetic, the range R0 from the antenna to the tile centre and the parameters derived from
+// it; the CTA then walks the pulses in batches, reading those parameters and staging the window
+// of compressed samples the tile can touch in shared memory (section 2.3 of the same page stages
+// echo data per image block the same way).  Long pulse ranges are split into slices (gridDim.z)
+// whose partial images a second kernel adds in slice order, so that small images and the last
+// wave still fill the GPU.
 //
 // Range and phase precision.  At X band the phase 4 pi R / lambda needs R to
 // ~1e-5 m at R ~ 6 km, beyond float32 (the listing in section 3.3 computes the
