@@ -717,7 +717,7 @@ def oracle_baseline(scene, cid, threads=None, full=False):
               f"{na} pulses and the {grid.nx}x{grid.ny} image")
     return {"value": round(pp / full_s / 1e9, 5), "unit": UNIT, "cores": n, "kind": "oracle",
             "sample": sample + f"; fp64, {n} thread{'s' if n > 1 else ''}", "cpu": cpu_model(),
-            "rc_s": round(rc_s, 3), "bp_s": round(bp_s, 3), "full_step_s": round(full_s, 2),
+            "rc_s": float(f"{rc_s:.4g}"), "bp_s": float(f"{bp_s:.4g}"), "full_step_s": float(f"{full_s:.4g}"),
             "extrapolated": not measured}
 
 

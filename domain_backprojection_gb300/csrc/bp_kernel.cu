@@ -39,6 +39,7 @@
 // 1 FMA + sin/cos on the SFU (phase), 4 FMA (complex multiply-accumulate).
 #include <cuda_fp16.h>
 #include <cstring>
+#include <type_traits>
 
 #include "sar_internal.cuh"
 
@@ -72,7 +73,7 @@ __device__ __forceinline__ unsigned entry_addr(unsigned base, float rnd)
 // lane of the CTA shares: (a, b, c, q0m), (c1, c2, c3, theta); each becomes a pair (x, x) in
 // registers (two loads per pulse instead of four of pre-duplicated pairs: measured on GB300,
 // 2.961 -> 2.914 ms on the spotlight scene, the compensated variant 3.129 -> 3.004 ms).
-template <bool kCheck>
+template <bool kCheck, bool kQuartic>
 __device__ __forceinline__ void pixel_pulse(const float4 *q4, const int4 wv, const unsigned base, const float2 ox2,
                                             const float2 *oyp, const float2 *odp, float2 *acc_r, float2 *acc_i,
                                             const BpArgs &args)
@@ -86,7 +87,7 @@ __device__ __forceinline__ void pixel_pulse(const float4 *q4, const int4 wv, con
 #pragma unroll
     for (int j = 0; j < kBpRowsPerThread / 2; j++) {
         const float2 g = __ffma2_rn(B2, oyp[j], __ffma2_rn(C2, odp[j], adx2));
-        float2 t = __ffma2_rn(g, __ffma2_rn(g, S3, S2), S1);
+        float2 t = kQuartic ? __ffma2_rn(g, __ffma2_rn(g, S3, S2), S1) : __ffma2_rn(g, S2, S1);
         t = __ffma2_rn(g, t, half2);
         const float2 qm = __ffma2_rn(g, t, QM2);
         const float2 rnd = __fadd2_rn(qm, magic2);
@@ -152,7 +153,7 @@ __device__ __forceinline__ void rotate_accumulate(const float2 vr, const float2 
 // (re, im) words.  With r = round(qm), the sample at q = qm + 1/2 is m_r + (qm - r) s_r: the
 // interpolation variable stays within [-1/2, 1/2], so no large intercept (the tau of the float32
 // entries) loses the float16 precision.  Arithmetic in float32.
-template <bool kCheck>
+template <bool kCheck, bool kQuartic>
 __device__ __forceinline__ void pixel_pulse_half(const float4 *q4, const int4 wv, const unsigned base, const float2 ox2,
                                                  const float2 *oyp, const float2 *odp, float2 *acc_r, float2 *acc_i,
                                                  const BpArgs &args)
@@ -166,7 +167,7 @@ __device__ __forceinline__ void pixel_pulse_half(const float4 *q4, const int4 wv
 #pragma unroll
     for (int j = 0; j < kBpRowsPerThread / 2; j++) {
         const float2 g = __ffma2_rn(B2, oyp[j], __ffma2_rn(C2, odp[j], adx2));
-        float2 t = __ffma2_rn(g, __ffma2_rn(g, S3, S2), S1);
+        float2 t = kQuartic ? __ffma2_rn(g, __ffma2_rn(g, S3, S2), S1) : __ffma2_rn(g, S2, S1);
         t = __ffma2_rn(g, t, half2v);
         const float2 qm = __ffma2_rn(g, t, QM2);
         const float2 rnd = __fadd2_rn(qm, magic2);
@@ -199,7 +200,7 @@ __device__ __forceinline__ void pixel_pulse_half(const float4 *q4, const int4 wv
 // which stays finite at f = 0 (only u_0 is nonzero there: the sample itself).  The taper W(f - k)
 // comes from one sin/cos of pi f / 4 by the angle-sum identity.  Staged entries are float32
 // samples; the row holds three samples before the window and four after.
-template <bool kCheck>
+template <bool kCheck, bool kQuartic>
 __device__ __forceinline__ void pixel_pulse_sinc(const float4 *q4, const int4 wv, const unsigned base, const float2 ox2,
                                                  const float2 *oyp, const float2 *odp, float2 *acc_r, float2 *acc_i,
                                                  const BpArgs &args)
@@ -218,7 +219,7 @@ __device__ __forceinline__ void pixel_pulse_sinc(const float4 *q4, const int4 wv
 #pragma unroll
     for (int j = 0; j < kBpRowsPerThread / 2; j++) {
         const float2 g = __ffma2_rn(B2, oyp[j], __ffma2_rn(C2, odp[j], adx2));
-        float2 t = __ffma2_rn(g, __ffma2_rn(g, S3, S2), S1);
+        float2 t = kQuartic ? __ffma2_rn(g, __ffma2_rn(g, S3, S2), S1) : __ffma2_rn(g, S2, S1);
         t = __ffma2_rn(g, t, half2v);
         const float2 qm = __ffma2_rn(g, t, QM2);
         const float2 rnd = __fadd2_rn(qm, magic2);
@@ -343,8 +344,12 @@ __device__ __forceinline__ dflt df_from_double(double v)
     return {hi, (float)(v - (double)hi)};
 }
 
+// Phase bound (radians) below which the series' quartic term is left out of a (tile, pulse).
+constexpr float kBpQuarticPhase = 1.0e-6f;
+
 // Per (tile, pulse) reference range (double-float) and window extent (float32), one thread each.
-// Output: pa = (a, b, c, q0m), pc = (c1, c2, c3, theta), win = (origin o, first entry, last entry, 0).
+// Output: pa = (a, b, c, q0m), pc = (c1, c2, c3, theta),
+// win = (origin o, first entry, last entry, 1 if the quartic term of the series is needed).
 // (ax, ay, az): the pulse's antenna position in double-float.
 __device__ __forceinline__ void tile_pulse_params(const BpArgs &args, int tile_x, int tile_y, const dflt ax,
                                                   const dflt ay, const dflt az, float4 &pa, float4 &pc, int4 &win)
@@ -394,13 +399,20 @@ __device__ __forceinline__ void tile_pulse_params(const BpArgs &args, int tile_x
     int e_hi = (int)floorf(fmaf(rmax - r0f, idr, qfrac)) + 2 + wh;
     e_lo = max(e_lo, 0);
     e_hi = min(e_hi, w - 1);
+    // Whether the pixel kernel needs the series' quartic term: over the tile |g| is at most
+    // G = |a| hx + |b| hy + c (hx^2 + hy^2), so the term moves a pixel's phase by at most
+    // 2 pi kappa |c3| G^4.  Below kBpQuarticPhase it is left out; that is far below the float32
+    // rounding of the phase argument (its last place is already 1e-6 rad at 8 rad).
+    const float gb = fabsf(pa.x) * hx + fabsf(pa.y) * hy + pa.z * fmaf(hx, hx, hy * hy);
+    int quartic = args.two_pi_kappa * fabsf(pc.z) * (gb * gb) * (gb * gb) > kBpQuarticPhase;
     if (!ok) {
         pa = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         pc = pa;
         e_lo = e_hi = wh;
+        quartic = 0;
         atomicOr(args.err, kDevErrGeometry);
     }
-    win = make_int4((int)o, e_lo, e_hi, 0);
+    win = make_int4((int)o, e_lo, e_hi, quartic);
 }
 
 // The parameter table: entry (tile, pulse) at table + 3 (tile_index * pulse_count + pulse - pulse_begin).
@@ -520,20 +532,31 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
     // Row sizes from the windows this CTA will actually stage (at most the diagonal bound w): the
     // widest window of the slice sets the stage row stride, and as many pulses as fit the shared
     // memory make a batch.
-    __shared__ int s_extent;
-    if (threadIdx.x == 0) s_extent = 1;
+    // The same scan finds whether any pulse of the slice needs the series' quartic term (the
+    // window's fourth word, set by the parameter kernel).
+    __shared__ int s_extent, s_quartic;
+    if (threadIdx.x == 0) {
+        s_extent = 1;
+        s_quartic = 0;
+    }
     __syncthreads();
     {
-        int m = 1;
+        int m = 1, need = 0;
         for (int n = p_begin + (int)threadIdx.x; n < p_end; n += kBpThreads) {
             const float4 wf = __ldg(tab + 3 * (int64_t)n + 2);
             m = max(m, __float_as_int(wf.z) - __float_as_int(wf.y) + 1);
+            need |= __float_as_int(wf.w);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) atomicMax(&s_extent, m);
+        need = __any_sync(0xffffffffu, need != 0);
+        if (lane == 0) {
+            atomicMax(&s_extent, m);
+            if (need) atomicOr(&s_quartic, 1);
+        }
     }
     __syncthreads();
+    const bool quartic = s_quartic != 0;
     const int stride = min(s_extent, args.w);                                // window entries per row
     const int row_n = kSinc ? ((stride + kExtra + 1) & ~1) : stride;        // stage entries per row
     const int rw = (stride + kExtra + 2) & ~1;                               // raw samples per row (even)
@@ -651,16 +674,22 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
         }
         cp_async_commit();
         // ---- pixel x pulse inner loop (four pulses unrolled, two with sinc interpolation: measured on
-        // GB300, spotlight scene 2.861 -> 2.847 ms against two; sinc 13.19 against 13.25 ms)
+        // GB300, spotlight scene 2.861 -> 2.847 ms against two; sinc 13.19 against 13.25 ms), in the
+        // form with or without the series' quartic term for the whole slice
+        auto pulse_loop = [&](auto tag) {
+            constexpr bool kQ = decltype(tag)::value;
 #pragma unroll(kPulseUnroll)
-        for (int p = 0; p < pb; p++) {
-            const int4 wv = win[p];
-            const unsigned base = stage_row0 + (unsigned)(p * row_n - wv.y + kTapsBefore) * kEb;
-            if constexpr (kSinc) pixel_pulse_sinc<kCheck>(quad + 2 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
-            else if constexpr (kMode == kBpHalfStage)
-                pixel_pulse_half<kCheck>(quad + 2 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
-            else pixel_pulse<kCheck>(quad + 2 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
-        }
+            for (int p = 0; p < pb; p++) {
+                const int4 wv = win[p];
+                const unsigned base = stage_row0 + (unsigned)(p * row_n - wv.y + kTapsBefore) * kEb;
+                if constexpr (kSinc) pixel_pulse_sinc<kCheck, kQ>(quad + 2 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
+                else if constexpr (kMode == kBpHalfStage)
+                    pixel_pulse_half<kCheck, kQ>(quad + 2 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
+                else pixel_pulse<kCheck, kQ>(quad + 2 * p, wv, base, ox2, oyp, odp, acc_r, acc_i, args);
+            }
+        };
+        if (quartic) pulse_loop(std::true_type{});
+        else pulse_loop(std::false_type{});
         if constexpr (kMode == kBpCompensated) {
 #pragma unroll
             for (int j = 0; j < kBpRowsPerThread / 2; j++) {

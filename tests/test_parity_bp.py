@@ -154,6 +154,32 @@ def test_squinted_grid(x_centre, monkeypatch):
     assert rel_l2(img_c.cpu().numpy(), img.cpu().numpy()) <= 1e-6
 
 
+def test_near_squinted_grid_needs_the_quartic_term(monkeypatch):
+    # 3.4 km slant range (the expansion's limit for these 128 x 16 tiles of 0.5 m pixels is 3.2 km)
+    # and a grid 1 km along track, 16 degrees of squint: the series' quartic term moves the phase
+    # by up to ~1e-4 rad at tile corners, so the pixel kernel must keep it (the scenes at 5.8 km
+    # stay below 1e-6 rad and leave it out); checked against the oracle with and without bounds
+    # checks
+    na = 64
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=na, prf=300.0 * na / 256, nx=48, ny=40,
+                              altitude=2000.0, ground_range=2800.0, fixed_target_offsets=((0, 0),))
+    s = synth.make_scene(cfg, device="cuda")
+    g = s["grid"]
+    grid = dataclasses.replace(g, x0=1000.0 - 0.5 * g.nx * g.dx)
+    plan = sar.sar_plan_create(s["radar"], grid, 0)
+    rc = sar.sar_range_compress(plan, s["raw"])
+    img = sar.sar_backproject(plan, rc, s["pos"])
+    sar.sar_plan_sync(plan)
+    ref = oracle.backproject(s["radar"], grid, rc.cpu().numpy(), s["pos"].cpu().numpy())
+    assert np.linalg.norm(ref) > 0.0
+    assert rel_l2(img.cpu().numpy(), ref) <= IMG_TOL
+    monkeypatch.setenv("SAR_CHECK_BOUNDS", "1")
+    checked = sar.sar_plan_create(s["radar"], grid, 0)
+    img_c = sar.sar_backproject(checked, rc, s["pos"])
+    sar.sar_plan_sync(checked)
+    assert rel_l2(img_c.cpu().numpy(), ref) <= IMG_TOL
+
+
 def test_window_edges_read_zero_outside_the_line():
     # a grid straddling the near and far ends of the compressed window: samples outside [0, U Nr) are zero
     s = _small_case(40, 40, na=32)
