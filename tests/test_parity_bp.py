@@ -328,10 +328,12 @@ def test_kernel_timing_records_each_call_and_leaves_results_unchanged():
     assert t == {"rc_ms": 0.0, "rc_calls": 0, "bp_ms": 0.0, "bp_calls": 0}
 
 
-def test_form_image_captures_into_a_cuda_graph():
+@pytest.mark.parametrize("cfg", [1, 3])
+def test_form_image_captures_into_a_cuda_graph(scene_cache, cfg):
     # sar_form_image enqueues its launches with no allocation or synchronisation, so a caller can
     # capture it into a CUDA graph and replay it on new echoes copied into the captured buffers
-    s = synth.make_scene(1, device="cuda")
+    # (the tiny scene, one pulse slice; the spotlight scene, eight slices and their sum)
+    s = scene_cache(cfg)
     plan = sar.sar_plan_create(s["radar"], s["grid"], 0)
     raw = s["raw"].clone()
     pos = s["pos"].clone()
@@ -345,7 +347,7 @@ def test_form_image_captures_into_a_cuda_graph():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         sar.sar_form_image(plan, raw, pos, image=img, workspace=ws)
-    other = synth.make_scene(dataclasses.replace(synth.SCENES[1], seed=91), device="cuda")
+    other = {"raw": torch.roll(s["raw"], 7, dims=0) * (0.5 - 0.25j), "pos": s["pos"] + 0.01}
     for scene in (s, other):
         raw.copy_(scene["raw"])
         pos.copy_(scene["pos"])
