@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
     constexpr bool kSinc = kMode == kBpSinc8;
     constexpr unsigned kEb = (kMode == kBpHalfStage || kSinc) ? 8u : 16u;
     constexpr int kTapsBefore = kSinc ? 3 : 0;
-    constexpr int kPulseUnroll = kSinc ? 2 : 4;
+    constexpr int kPulseUnroll = kSinc ? 2 : 8;
     constexpr int kExtra = kSinc ? 7 : 1;                       // raw samples per row beyond its entries
     extern __shared__ float4 smem4[];
     constexpr int kWarps = kBpThreads / 32;
@@ -673,9 +673,11 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
             cp_async16((unsigned)__cvta_generic_to_shared(wins + pb_cap * buf2 + threadIdx.x), src + 2);
         }
         cp_async_commit();
-        // ---- pixel x pulse inner loop (four pulses unrolled, two with sinc interpolation: measured on
-        // GB300, spotlight scene 2.861 -> 2.847 ms against two; sinc 13.19 against 13.25 ms), in the
-        // form with or without the series' quartic term for the whole slice
+        // ---- pixel x pulse inner loop, in the form with or without the series' quartic term for the
+        // whole slice.  Eight pulses unrolled, two with sinc interpolation (measured on GB300, pixel
+        // kernel on the spotlight scene: 2.720 ms with four, 2.691 with eight, 2.830 with twelve,
+        // 2.762 with sixteen; curved-track scene 43.31 ms with four, 42.46 with eight.  Sinc, two:
+        // 13.19 against 13.25 ms)
         auto pulse_loop = [&](auto tag) {
             constexpr bool kQ = decltype(tag)::value;
 #pragma unroll(kPulseUnroll)
