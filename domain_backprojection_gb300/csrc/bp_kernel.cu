@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
     constexpr bool kSinc = kMode == kBpSinc8;
     constexpr unsigned kEb = (kMode == kBpHalfStage || kSinc) ? 8u : 16u;
     constexpr int kTapsBefore = kSinc ? 3 : 0;
-    constexpr int kPulseUnroll = kSinc ? 2 : 8;
+    constexpr int kPulseUnroll = kMode == kBpLinear ? 8 : 4;           // pulses per unrolled loop step
     constexpr int kExtra = kSinc ? 7 : 1;                       // raw samples per row beyond its entries
     extern __shared__ float4 smem4[];
     constexpr int kWarps = kBpThreads / 32;
@@ -674,10 +674,12 @@ __global__ void __launch_bounds__(kBpThreads, bp_mode_ctas(kMode)) bp_kernel(BpA
         }
         cp_async_commit();
         // ---- pixel x pulse inner loop, in the form with or without the series' quartic term for the
-        // whole slice.  Eight pulses unrolled, two with sinc interpolation (measured on GB300, pixel
-        // kernel on the spotlight scene: 2.720 ms with four, 2.691 with eight, 2.830 with twelve,
-        // 2.762 with sixteen; curved-track scene 43.31 ms with four, 42.46 with eight.  Sinc, two:
-        // 13.19 against 13.25 ms)
+        // whole slice.  Eight pulses unrolled in the default variant, four in the others (measured on
+        // GB300, spotlight scene: pixel kernel 2.720 ms with four, 2.691 with eight, 2.830 with
+        // twelve, 2.762 with sixteen, curved-track scene 43.31 ms with four and 42.46 with eight;
+        // whole backprojection calls, four against eight: compensated 2.916 against 2.947 ms,
+        // float16 stage 3.538 against 3.551 ms; sinc, four against two and one: 13.157 against
+        // 13.176 and 13.218 ms)
         auto pulse_loop = [&](auto tag) {
             constexpr bool kQ = decltype(tag)::value;
 #pragma unroll(kPulseUnroll)
