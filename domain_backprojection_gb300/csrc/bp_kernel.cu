@@ -25,7 +25,10 @@
 //     R - R0 = g/2 - g^2/(8 R0) + g^3/(16 R0^2) - 5 g^4/(128 R0^3) + O(g^5/R0^4),
 // evaluated by Horner's rule in range-bin units (the binomial series of
 // R0 sqrt(1 + g/R0)).  |d| <= h (the tile half-diagonal, at most 32 m) and R0 >= 100 h
-// keep the truncation below 9e-9 h, 3e-7 m (below 1e-9 m for 16 m tiles at 5.8 km).
+// keep the truncation below 9e-9 h, 3e-7 m (below 1e-9 m for 16 m tiles at 5.8 km).  The
+// quartic term is evaluated only by CTAs whose slice has a (tile, pulse) where it can move the
+// phase by 1e-6 rad or more (the prep kernel bounds it); elsewhere it is far below the float32
+// rounding of the phase and the loop leaves it out.
 //
 // Interpolation and phase in one staged pair.  With q the pixel's fractional
 // bin relative to the window origin o (half a bin shifted: qm = q - 1/2) and
@@ -34,9 +37,10 @@
 // tau_i = v_i - (i - 1/2) sigma_i.  The phase is 2 pi [(2/lambda) R_start +
 // kappa (o + 1/2)] + 2 pi kappa qm, kappa = 2 dr / lambda, so the per-(tile,
 // pulse) part is one angle theta and the per-pixel part one fused multiply-add.
-// Per pixel and pulse that leaves: 2 FMA (range offset), 4 FMA (series),
-// 1 add (round), 1 integer op (address), 1 shared 128-bit load, 2 FMA (interp),
-// 1 FMA + sin/cos on the SFU (phase), 4 FMA (complex multiply-accumulate).
+// Per pixel and pulse that leaves: 2 FMA (range offset), 3 FMA (series; 4 with the quartic
+// term), 1 add (round), 1 integer op (address), 1 shared 128-bit load, 2 FMA (interp),
+// 1 FMA + sin/cos on the SFU (phase), 4 FMA (complex multiply-accumulate); the FMAs and adds of
+// two pixel rows go as one paired instruction.
 #include <cuda_fp16.h>
 #include <cstring>
 #include <type_traits>
