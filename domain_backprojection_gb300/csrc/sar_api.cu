@@ -420,16 +420,29 @@ sar_status setup_bp(sar_plan p)
     // rest for raw and staged rows; the kernel sizes its rows from the windows it actually stages
     const int pulses_per_batch = 48;
     const int stage_bytes = 216 * 1024 / sar::kBpCtasPerSm - sar::kBpParamSlots * pulses_per_batch * (int)sizeof(float4);
-    a.tile_w = 32;
-    for (int tw : {128, 64}) {
+    // When no shape stays within h_max: the one with the smallest half-diagonal, and of equal ones
+    // the longest in azimuth.  Pixels carry their range as a float32 offset from the tile centre, so
+    // a tile short in range also keeps the offsets' rounding small: at X band about 1.5e-3 rad of
+    // phase for the 27 m range half-extent of a 32 x 64 tile of 1 m pixels, half that for 64 x 32
+    // (measured against the oracle on images of noise, where it shows undamped).
+    a.tile_w = 0;
+    int fallback_w = 32;
+    double fallback_h = 1e300;
+    for (int tw : {128, 64, 32}) {
         const int th = sar::kBpThreads * sar::kBpRowsPerThread / tw;
         const double h = 0.5 * std::hypot((tw - 1) * g.dx, (th - 1) * g.dy);
         const int w = 2 * ((int)std::ceil(h / dr) + 3) + 1;
-        if (h <= h_max && w * 16 + ((w + 3) & ~1) * 8 <= stage_bytes) {
+        if (w * 16 + ((w + 3) & ~1) * 8 > stage_bytes) continue;
+        if (h <= h_max) {
             a.tile_w = tw;
             break;
         }
+        if (h < fallback_h) {
+            fallback_h = h;
+            fallback_w = tw;
+        }
     }
+    if (a.tile_w == 0) a.tile_w = fallback_w;
     a.tile_h = sar::kBpThreads * sar::kBpRowsPerThread / a.tile_w;
     a.tiles_x = (g.nx + a.tile_w - 1) / a.tile_w;
     a.tiles_y = (g.ny + a.tile_h - 1) / a.tile_h;
