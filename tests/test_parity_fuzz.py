@@ -59,3 +59,51 @@ def test_random_configuration(case):
     print(f"case {case}: Nr {n_range} U {upsample} pixel {pixel} m, {nx} x {ny}, pulses {p0}+{cnt} of {na}: "
           f"image rel L2 {err:.2e}")
     assert err <= IMG_TOL
+
+
+# per case: line length, upsampling, pixel spacing (m), along-track grid offset (m), pixel-kernel variant
+MODE_CASES = [(4095, 8, 0.5, 0.0, "sinc8"), (5003, 2, 0.5, 300.0, "linear"), (8192, 8, 0.25, -200.0, "compensated"),
+              (6000, 4, 0.5, 1200.0, "fp16_stage"), (4096, 1, 0.2, 0.0, "sinc8"), (2000, 8, 0.3, -1500.0, "linear"),
+              (1536, 2, 0.75, 600.0, "compensated"), (3000, 8, 0.4, -800.0, "fp16_stage")]
+_MODE_SET = {
+    "linear": (lambda p: None, oracle.INTERP_LINEAR),
+    "compensated": (lambda p: sar.sar_plan_set_accumulation(p, sar.SAR_ACCUM_COMPENSATED), oracle.INTERP_LINEAR),
+    "fp16_stage": (lambda p: sar.sar_plan_set_stage_precision(p, sar.SAR_STAGE_FP16), oracle.INTERP_LINEAR),
+    "sinc8": (lambda p: sar.sar_plan_set_interpolation(p, sar.SAR_INTERP_SINC8), oracle.INTERP_SINC8),
+}
+
+
+@pytest.mark.parametrize("case", range(len(MODE_CASES)))
+def test_random_configuration_variants(case):
+    # the pixel-kernel variants and the longer line paths (Bluestein up to 4096 and above it, the
+    # staged 8192-point kernel, 6000 points) on squinted grids, through sar_form_image (polyphase
+    # planes), against the oracle's compressed lines and its image of those lines with the
+    # variant's interpolation
+    n_range, upsample, pixel, x_off, mode = MODE_CASES[case]
+    rng = np.random.default_rng(8000 + case)
+    na = int(rng.choice([16, 24, 32]))
+    nx, ny = int(rng.integers(1, 60)), int(rng.integers(1, 60))
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=na, n_range=n_range, upsample=upsample,
+                              prf=300.0 * na / 256, nx=nx, ny=ny, pixel=pixel,
+                              fixed_target_offsets=((0, 0),), seed=9500 + case)
+    s = synth.make_scene(cfg, device="cuda")
+    radar, g = s["radar"], s["grid"]
+    grid = dataclasses.replace(g, x0=g.x0 + x_off + 0.29 * pixel, y0=g.y0 + float(rng.uniform(-10.0, 10.0)))
+    plan = sar.sar_plan_create(radar, grid, 0)
+    _MODE_SET[mode][0](plan)
+    img = sar.sar_form_image(plan, s["raw"], s["pos"])
+    sar.sar_plan_sync(plan)
+    # the same plan's compressed lines, in natural order, for the image reference
+    sar.sar_plan_set_rc_layout(plan, sar.SAR_RC_NATURAL)
+    rc = sar.sar_range_compress(plan, s["raw"])
+    sar.sar_plan_sync(plan)
+    got_rc = rc.cpu().numpy()
+    ref_rc = oracle.range_compress(radar, s["raw"].cpu().numpy(), threads=ORACLE_THREADS)
+    assert rel_l2(got_rc, ref_rc) <= RC_TOL
+    ref = oracle.backproject(radar, grid, got_rc.astype(np.complex64), s["pos"].cpu().numpy(),
+                             threads=ORACLE_THREADS, interp=_MODE_SET[mode][1])
+    assert np.linalg.norm(ref) > 0.0
+    err = rel_l2(img.cpu().numpy(), ref)
+    print(f"variant case {case}: Nr {n_range} U {upsample} pixel {pixel} m, {nx} x {ny}, x offset {x_off} m, "
+          f"{mode}: image rel L2 {err:.2e}")
+    assert err <= IMG_TOL
