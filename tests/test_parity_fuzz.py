@@ -9,6 +9,7 @@ import dataclasses
 
 import numpy as np
 import pytest
+import torch
 
 import domain_backprojection_gb300 as sar
 import oracle
@@ -106,4 +107,42 @@ def test_random_configuration_variants(case):
     err = rel_l2(img.cpu().numpy(), ref)
     print(f"variant case {case}: Nr {n_range} U {upsample} pixel {pixel} m, {nx} x {ny}, x offset {x_off} m, "
           f"{mode}: image rel L2 {err:.2e}")
+    assert err <= IMG_TOL
+
+
+# per case: pulses, line length, upsampling, range window, pulse weights
+HOST_CASES = [(512, 1024, 8, "hamming", True), (640, 600, 4, "taylor", False), (768, 512, 2, "none", True),
+              (544, 1000, 8, "taylor", True)]
+
+
+@pytest.mark.parametrize("case", range(len(HOST_CASES)))
+def test_random_configuration_host_path(case):
+    # sar_form_image_host (pulses copied in chunks that overlap the kernels, from pinned host
+    # buffers) with a weighted matched filter and random pulse weights, against the oracle's
+    # weighted compression of the same echoes and its image of those lines scaled by the weights
+    na, n_range, upsample, window, weighted = HOST_CASES[case]
+    rng = np.random.default_rng(8500 + case)
+    nx, ny = int(rng.integers(8, 48)), int(rng.integers(8, 48))
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=na, n_range=n_range, upsample=upsample,
+                              prf=300.0 * na / 256, nx=nx, ny=ny, fixed_target_offsets=((0, 0), (3, -2)),
+                              seed=9700 + case)
+    s = synth.make_scene(cfg, device="cuda")
+    radar, grid = s["radar"], s["grid"]
+    plan = sar.sar_plan_create(radar, grid, 0)
+    win = {"none": (sar.SAR_WINDOW_NONE, oracle.WINDOW_NONE), "hamming": (sar.SAR_WINDOW_HAMMING, oracle.WINDOW_HAMMING),
+           "taylor": (sar.SAR_WINDOW_TAYLOR, oracle.WINDOW_TAYLOR)}[window]
+    sar.sar_plan_set_range_window(plan, win[0])
+    w = None
+    if weighted:
+        w = torch.tensor(rng.uniform(0.5, 1.5, na), dtype=torch.float32, device="cuda")
+        sar.sar_plan_set_pulse_weights(plan, w)
+    img = sar.sar_form_image_host(plan, s["raw"].cpu().pin_memory(), s["pos"].cpu().pin_memory())
+    sar.sar_plan_sync(plan)
+    rc = oracle.range_compress(radar, s["raw"].cpu().numpy(), threads=ORACLE_THREADS, window=win[1])
+    if weighted:
+        rc = rc * w.cpu().numpy()[:, None]
+    ref = oracle.backproject(radar, grid, rc, s["pos"].cpu().numpy(), threads=ORACLE_THREADS)
+    err = rel_l2(img.numpy(), ref)
+    print(f"host case {case}: {na} pulses, Nr {n_range} U {upsample}, {window} window, weights {weighted}, "
+          f"{nx} x {ny}: image rel L2 {err:.2e}")
     assert err <= IMG_TOL
