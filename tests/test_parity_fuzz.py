@@ -146,3 +146,28 @@ def test_random_configuration_host_path(case):
     print(f"host case {case}: {na} pulses, Nr {n_range} U {upsample}, {window} window, weights {weighted}, "
           f"{nx} x {ny}: image rel L2 {err:.2e}")
     assert err <= IMG_TOL
+
+
+# per case: pulses (a power of two), line length, PRF (Hz)
+RD_CASES = [(512, 1024, 200.0), (1024, 600, 900.0), (2048, 512, 2500.0), (512, 4096, 350.0)]
+
+
+@pytest.mark.parametrize("case", range(len(RD_CASES)))
+def test_random_configuration_range_doppler(case):
+    # range-Doppler image formation at random pulse counts, line lengths (one a mixed radix) and pulse
+    # spacings (so that the range migration and its step between neighbouring range bins vary),
+    # against the oracle's range-Doppler image of the same echoes
+    na, n_range, prf = RD_CASES[case]
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=na, n_range=n_range, upsample=1, prf=prf,
+                              nx=64, ny=64, fixed_target_offsets=((0, 0), (10, -6)), seed=9800 + case)
+    s = synth.make_scene(cfg, device="cuda")
+    radar, du = s["radar"], cfg.velocity / cfg.prf
+    plan = sar.sar_plan_create(radar, None, 0)
+    sar.sar_plan_set_range_doppler(plan, du)
+    img = sar.sar_range_doppler(plan, s["raw"])
+    sar.sar_plan_sync(plan)
+    rc = oracle.range_compress(radar, s["raw"].cpu().numpy(), threads=ORACLE_THREADS)
+    ref = oracle.range_doppler(radar, rc, du, threads=ORACLE_THREADS)
+    err = rel_l2(img.cpu().numpy(), ref)
+    print(f"range-Doppler case {case}: {na} pulses, Nr {n_range}, pulse spacing {du:.3f} m: image rel L2 {err:.2e}")
+    assert err <= IMG_TOL
