@@ -403,17 +403,20 @@ def test_pulse_weights():
 def test_tile_shape_follows_the_range_bound():
     # the plan picks the longest azimuth tile whose half-diagonal h stays within
     # clamp(R_start / 150, 20 m, 32 m): 128 x 16 pixels at 0.5 m (h = 32 m) for the small scene's
-    # 4978 m window start, 64 x 32 (h = 17.6 m) when the window starts at 1500 m
+    # 4978 m window start, 64 x 32 (h = 17.6 m) when the window starts at 1500 m; with 1 m pixels no
+    # shape stays within 32 m, and of the two with the smallest h (35 m) the longer in azimuth,
+    # 64 x 32, keeps the range offsets short
     import os
     import re
     import subprocess
     import sys
     code = ("import dataclasses, synth, domain_backprojection_gb300 as sar; c = synth.SCENES[2]; "
             "sar.sar_plan_create(c.radar(), c.grid(), 0); "
-            "sar.sar_plan_create(dataclasses.replace(c.radar(), range_start=1500.0), c.grid(), 0)")
+            "sar.sar_plan_create(dataclasses.replace(c.radar(), range_start=1500.0), c.grid(), 0); "
+            "sar.sar_plan_create(c.radar(), dataclasses.replace(c.grid(), dx=1.0, dy=1.0), 0)")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=dict(os.environ, SAR_LOG="1"),
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     shapes = re.findall(r"tiles \d+ x \d+ of (\d+) x (\d+) pixels", r.stderr)
-    assert shapes == [("128", "16"), ("64", "32")], r.stderr
+    assert shapes == [("128", "16"), ("64", "32"), ("64", "32")], r.stderr
