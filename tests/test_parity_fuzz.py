@@ -171,3 +171,36 @@ def test_random_configuration_range_doppler(case):
     err = rel_l2(img.cpu().numpy(), ref)
     print(f"range-Doppler case {case}: {na} pulses, Nr {n_range}, pulse spacing {du:.3f} m: image rel L2 {err:.2e}")
     assert err <= IMG_TOL
+
+
+# per case: line length, upsampling, pixel spacing (m), which end of the window, pixel-kernel variant
+EDGE_CASES = [(1024, 8, 0.5, "near", "sinc8"), (1000, 2, 0.25, "far", "linear"), (512, 4, 0.75, "near", "fp16_stage"),
+              (2048, 1, 0.3, "far", "sinc8")]
+
+
+@pytest.mark.parametrize("case", range(len(EDGE_CASES)))
+def test_random_configuration_window_edges(case):
+    # grids straddling the near or far end of the compressed window: every row's gather runs past
+    # the line and must read zeros there (the sinc rows three samples before and four after), in
+    # each variant
+    n_range, upsample, pixel, end, mode = EDGE_CASES[case]
+    rng = np.random.default_rng(8700 + case)
+    na = int(rng.choice([16, 32]))
+    nx, ny = int(rng.integers(4, 40)), int(rng.integers(20, 60))
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=na, n_range=n_range, upsample=upsample,
+                              prf=300.0 * na / 256, nx=nx, ny=ny, pixel=pixel, seed=9900 + case)
+    s = synth.make_scene(cfg, device="cuda")
+    radar, g = s["radar"], s["grid"]
+    edge = radar.range_start + (0.0 if end == "near" else n_range * synth.C0 / (2 * radar.fs))
+    y_edge = float(np.sqrt(edge ** 2 - cfg.altitude ** 2))
+    grid = dataclasses.replace(g, y0=y_edge - (ny // 2) * pixel + float(rng.uniform(-1.0, 1.0)))
+    plan = sar.sar_plan_create(radar, grid, 0)
+    _MODE_SET[mode][0](plan)
+    rc = sar.sar_range_compress(plan, s["raw"])
+    img = sar.sar_backproject(plan, rc, s["pos"])
+    sar.sar_plan_sync(plan)
+    ref = oracle.backproject(radar, grid, rc.cpu().numpy(), s["pos"].cpu().numpy(), threads=ORACLE_THREADS,
+                             interp=_MODE_SET[mode][1])
+    err = np.linalg.norm(img.cpu().numpy() - ref) / max(np.linalg.norm(ref), 1e-3)
+    print(f"edge case {case}: Nr {n_range} U {upsample} pixel {pixel} m, {end} end, {mode}: image rel L2 {err:.2e}")
+    assert err <= IMG_TOL
