@@ -386,14 +386,22 @@ def profile_case(case="spotlight"):
     import synth
 
     if case.startswith("sweep"):
-        nr = int(case[len("sweep"):])
-        sc = synth.make_rc_sweep(nr, n_lines=4096, device="cuda")
-        plan = sar.sar_plan_create(sc["radar"], None, 0)
-        out = torch.empty_like(sc["raw"])
+        # sweepNR: 4096 lines of NR samples, U = 1; sweepNRuU: 2048 lines with upsampling by U into
+        # polyphase planes (the large scene's line kernel on a case small enough for a full capture)
+        spec = case[len("sweep"):]
+        nr, U = (int(spec.split("u")[0]), int(spec.split("u")[1])) if "u" in spec else (int(spec), 1)
+        lines = 4096 if U == 1 else 2048
+        sc = synth.make_rc_sweep(nr, n_lines=lines, device="cuda")
+        import dataclasses
+        radar = dataclasses.replace(sc["radar"], upsample=U)
+        plan = sar.sar_plan_create(radar, None, 0)
+        if U > 1:
+            sar.sar_plan_set_rc_layout(plan, sar.SAR_RC_POLYPHASE)
+        out = torch.empty(lines, nr * U, dtype=torch.complex64, device="cuda")
         for _ in range(3):
             sar.sar_range_compress(plan, sc["raw"], out)
         sar.sar_plan_sync(plan)
-        print(json.dumps({"profile_case": "ok", "workload": f"range-only sweep, 4096 lines of {nr} samples, U=1"}))
+        print(json.dumps({"profile_case": "ok", "workload": f"range-only sweep, {lines} lines of {nr} samples, U={U}"}))
         return
     if case == "rda":
         import dataclasses
