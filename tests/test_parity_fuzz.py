@@ -204,3 +204,37 @@ def test_random_configuration_window_edges(case):
     err = np.linalg.norm(img.cpu().numpy() - ref) / max(np.linalg.norm(ref), 1e-3)
     print(f"edge case {case}: Nr {n_range} U {upsample} pixel {pixel} m, {end} end, {mode}: image rel L2 {err:.2e}")
     assert err <= IMG_TOL
+
+
+# per case: line length, chirp duration (s), upsampling, pulses, grid (nx, ny)
+SHORT_CASES = [(64, 0.1e-6, 8, 512, (3, 200)), (100, 0.2e-6, 4, 256, (200, 1)), (250, 0.5e-6, 2, 1024, (9, 9)),
+               (16, 0.05e-6, 1, 64, (40, 40))]
+
+
+@pytest.mark.parametrize("case", range(len(SHORT_CASES)))
+def test_random_configuration_short_lines(case):
+    # short lines of short chirps (the shared-memory mixed-radix kernel at 16..250 samples), extreme
+    # grid aspects and many pulses on few pixels (the most pulse slices), against the oracle
+    from synth.scenes import add_echoes, targets, track
+    n_range, tp, upsample, na, (nx, ny) = SHORT_CASES[case]
+    cfg = dataclasses.replace(synth.SCENES[1], n_pulses=na, n_range=n_range, upsample=upsample,
+                              prf=300.0 * na / 256, nx=nx, ny=ny, fixed_target_offsets=((0, 0),), seed=9950 + case)
+    radar = dataclasses.replace(cfg.radar(), pulse_width=tp)
+    grid = cfg.grid()
+    pos = track(cfg, "cuda")
+    raw = torch.zeros(na, n_range, dtype=torch.complex64, device="cuda")
+    xyz, amp, _ = targets(cfg)
+    add_echoes(raw, pos, xyz, amp, radar)
+    g = torch.Generator(device="cuda").manual_seed(123 + case)
+    raw += 0.05 * torch.complex(torch.randn(na, n_range, generator=g, device="cuda"),
+                                torch.randn(na, n_range, generator=g, device="cuda"))
+    plan = sar.sar_plan_create(radar, grid, 0)
+    img = sar.sar_form_image(plan, raw, pos)
+    sar.sar_plan_sync(plan)
+    rc = oracle.range_compress(radar, raw.cpu().numpy(), threads=ORACLE_THREADS)
+    ref = oracle.backproject(radar, grid, rc, pos.cpu().numpy(), threads=ORACLE_THREADS)
+    assert np.linalg.norm(ref) > 0.0
+    err = rel_l2(img.cpu().numpy(), ref)
+    print(f"short case {case}: Nr {n_range} ({round(tp * radar.fs)}-sample chirp) U {upsample}, {na} pulses, "
+          f"{nx} x {ny}: image rel L2 {err:.2e}")
+    assert err <= IMG_TOL
